@@ -1,0 +1,481 @@
+"""Benchmark of batched quintic Newton–Schulz on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-per-shape] [--no-cpu-baseline]
+
+A "step" is one whole NS call (norm, scale, then 5 x Gram / polynomial /
+update) over the workload's stack, inputs resident in HBM.  The default
+workload is the 128-expert MoE stack 128 x 1536 x 2048 (bf16), one of the two
+shapes the method is held to 60% of dense bf16 peak on; every other workload
+is timed briefly under "per_shape".  Rank 0 prints one JSON line.
+
+N > 1 (torchrun): each rank runs the same workload on its own GPU with no
+collective in the data path (the NS of a stack does not shard across GPUs
+here: replicas only); a barrier brackets the timed region and the time is the
+maximum over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (one matrix per step, scaled to a whole call).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import ns_inputs  # noqa: E402
+
+METRIC = "ms per NS call and dense-equiv TFLOP/s (% of GB300 bf16 peak), per shape"
+DEFAULT_WORKLOAD = "experts_128x1536x2048"
+L2_BYTES = 129 * 1024 * 1024
+PAGES_H200_QUACK_MS = {  # prime-rl PR #3873, Results, "NS microbenchmark on one H200" (context only)
+    "square_4096": 2.71, "square_8192": 17.0, "wide_4096x14336": 7.07,
+    "experts_128x1536x2048": 25.0, "stack_128x2048x768": 8.6, "stack_32x7168x2048": 33.0,
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "newton_schulz_07_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, or None
+    when it is absent or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    ent = rec.get("kernels", {}).get(workload, {}).get(kernel)
+    return None if ent is None else float(ent["dram_bytes_per_launch"])
+
+
+def flop_counts(w, steps=5):
+    """Per-launch useful FLOPs of each tensor-core kernel and the dense-
+    equivalent total of one call."""
+    m, n, b = float(w.m), float(w.n), float(w.batch)
+    return {
+        "gram": b * m * (m + 1) * n,
+        "poly": b * m * m * (m + 1),
+        "update": b * 2 * m * m * n,
+        "normalize_bytes": b * 6.0 * w.rows * w.cols,
+        "dense_call": w.dense_flops(steps),
+        "useful_call": w.useful_flops(steps),
+    }
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            n += 1
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": n}
+
+
+def gpu_id_for(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return str(dev)
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0]), "blas threadpool"
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var]), var
+    return len(os.sched_getaffinity(0)), "affinity (BLAS default: all cores)"
+
+
+def oracle_one(w, k):
+    import oracle
+    g = ns_inputs.bf16_bits_to_f64(ns_inputs.matrix_bits(w, k))
+    t0 = time.perf_counter()
+    oracle.newton_schulz(g)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle as it stands on a bounded sample of the workload: whole
+    matrices, as many as fit in about `budget_s` seconds, scaled to a call."""
+    times = [oracle_one(w, 0)]
+    k = 1
+    while sum(times) < budget_s and k < w.batch:
+        times.append(oracle_one(w, k))
+        k += 1
+    per_matrix = sum(times) / len(times)
+    cores, src = cpu_threads()
+    return {"value": per_matrix * w.batch * 1e3, "unit": "ms", "cores": cores, "cores_source": src,
+            "kind": "oracle",
+            "sample": f"{len(times)} of {w.batch} matrices ({w.rows}x{w.cols}) of {w.name}, fp64 numpy oracle, "
+                      f"{sum(times):.1f} s, scaled by {w.batch}/{len(times)}"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = ns_inputs.WORKLOADS[args.workload]
+    for i in range(args.warmup):
+        oracle_one(w, i % w.batch)
+    times = []
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        times.append(oracle_one(w, (args.warmup + i) % w.batch) * w.batch)
+    wall = time.perf_counter() - t_all
+    ms = 1e3 * sum(times) / len(times)
+    cores, src = cpu_threads()
+    fl = flop_counts(w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "rows": w.rows, "cols": w.cols, "ns_steps": 5,
+                   "parallelism": "host cores"},
+        "tflops_dense_equiv": fl["dense_call"] / (ms * 1e-3) / 1e12,
+        "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "cores_source": src, "kind": "oracle",
+                         "sample": f"each step: 1 of {w.batch} matrices ({w.rows}x{w.cols}) through the fp64 "
+                                   f"numpy oracle, scaled by {w.batch}; {args.steps} steps in {wall:.1f} s"},
+        "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ns_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-per-shape", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+
+    import newton_schulz_07_gb300 as ns
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peaks, peak_src = load_peaks()
+    w = ns_inputs.WORKLOADS[args.workload]
+    fl = flop_counts(w)
+
+    bits = ns_inputs.stack_bits(w)
+    host_in = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    G = host_in.to(dev)
+    out = torch.empty_like(G)
+    ws = ns.alloc_workspace(w.batch, w.rows, w.cols, device=dev)
+    working_set = 2 * G.numel() * 2 + ws.numel()
+    flush = working_set < 4 * L2_BYTES
+    scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        ns.muon_ns(G, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if scrub is not None:
+            scrub.fill_(i & 0xFF)
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    barrier()
+    ms_local = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ms = max_over_ranks(ms_local)
+    dev_err = ns.read_error(ws)
+
+    # Per-kernel breakdown: the same kernels through the per-step entry points,
+    # CUDA events on the launching stream between launches.
+    nb = min(args.steps, 20)
+    names = ["normalize", "gram", "poly", "update"]
+    acc = {k: 0.0 for k in names}
+    a_buf = torch.empty((w.batch, w.m, w.m), dtype=torch.bfloat16, device=dev)
+    b_buf = torch.empty_like(a_buf)
+    x_bufs = [torch.empty_like(G), torch.empty_like(G)]
+    err_word = torch.zeros(1, dtype=torch.int32, device=dev)
+    a, b, c = ns.DEFAULT_COEFFS
+    for it in range(nb + 2):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
+        ev[0].record(stream)
+        ns.muon_ns_normalize(G, ws, X=x_bufs[0])
+        ev[1].record(stream)
+        cur = 0
+        for s in range(5):
+            ns.muon_ns_gram(x_bufs[cur], A=a_buf, device_error=err_word)
+            ev[2 + 3 * s].record(stream)
+            ns.muon_ns_poly(a_buf, b, c, B=b_buf, device_error=err_word)
+            ev[3 + 3 * s].record(stream)
+            ns.muon_ns_update(x_bufs[cur], b_buf, a, Xn=x_bufs[1 - cur], device_error=err_word)
+            ev[4 + 3 * s].record(stream)
+            cur = 1 - cur
+        torch.cuda.synchronize()
+        if it < 2:
+            continue
+        acc["normalize"] += ev[0].elapsed_time(ev[1])
+        for s in range(5):
+            acc["gram"] += ev[1 + 3 * s].elapsed_time(ev[2 + 3 * s]) / 5
+            acc["poly"] += ev[2 + 3 * s].elapsed_time(ev[3 + 3 * s]) / 5
+            acc["update"] += ev[3 + 3 * s].elapsed_time(ev[4 + 3 * s]) / 5
+    per_launch_ms = {k: v / nb for k, v in acc.items()}
+    share = {"normalize": per_launch_ms["normalize"]}
+    for k in ("gram", "poly", "update"):
+        share[k] = 5 * per_launch_ms[k]
+    dominant = max(("gram", "poly", "update"), key=lambda k: share[k])
+    achieved = fl[dominant] / (per_launch_ms[dominant] * 1e-3) / 1e12
+    traffic = recorded_traffic(dominant, w.name)
+    roofline = {"bound": "tensor", "kernel": f"ns_tc_gemm ({dominant})", "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
+                "traffic": traffic,
+                "algorithmic_flops_per_launch": fl[dominant],
+                "avg_launch_ms": per_launch_ms[dominant]}
+    norm_gbs = fl["normalize_bytes"] / (per_launch_ms["normalize"] * 1e-3) / 1e9
+    breakdown = {
+        "per_launch_ms": per_launch_ms,
+        "per_call_ms": share,
+        "normalize_hbm": {"achieved_gbs": norm_gbs, "peak_gbs": peaks["hbm_gbs"],
+                          "frac": norm_gbs / peaks["hbm_gbs"], "bytes_per_call": fl["normalize_bytes"]},
+        "tensor_tflops_useful": {k: fl[k] / (per_launch_ms[k] * 1e-3) / 1e12 for k in ("gram", "poly", "update")},
+    }
+
+    # End to end through the public API with host buffers: pinned H2D of the
+    # input, the NS call, D2H of the result, every step.
+    host_out = torch.empty_like(host_in).pin_memory()
+    ne = min(args.steps, 20)
+    G.copy_(host_in, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ne):
+        G.copy_(host_in, non_blocking=True)
+        ns.muon_ns(G, out=out, workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne)
+    io_bytes = G.numel() * 2
+
+    # Spot parity of the timed call's output (untimed; matrix 0 vs the oracle).
+    parity = None
+    if rank == 0:
+        import oracle
+        got = ns_inputs.bf16_bits_to_f64(host_out[0].view(torch.int16).numpy().view(np.uint16))
+        ref = oracle.newton_schulz(ns_inputs.bf16_bits_to_f64(bits[0]))
+        parity = {"matrix": 0, "rel_fro_err_vs_fp64_oracle": float(np.linalg.norm(got - ref) / np.linalg.norm(ref)),
+                  "tolerance": 1.5e-2}
+
+    per_shape = None
+    if not args.no_per_shape and world == 1:
+        per_shape = {}
+        del a_buf, b_buf, x_bufs
+        for name, ow in ns_inputs.WORKLOADS.items():
+            if name == w.name:
+                continue
+            per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        tf_dense = fl["dense_call"] / (ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": ms / PAGES_H200_QUACK_MS[w.name] if w.name in PAGES_H200_QUACK_MS else None,
+            "vs_baseline_note": "ms ratio to the pages' H200 QuACK figure for this shape (another GPU; context)",
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "rows": w.rows, "cols": w.cols, "ns_steps": 5,
+                       "coeffs": list(ns.DEFAULT_COEFFS), "eps": ns.DEFAULT_EPS,
+                       "distribution": w.dist, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": ("flushed between timed steps (256 MiB write)" if flush else
+                              f"working set {working_set / 2**30:.1f} GiB >> L2, no flush")},
+            "tflops_dense_equiv": tf_dense,
+            "tflops_useful": fl["useful_call"] / (ms * 1e-3) / 1e12,
+            "pct_dense_bf16_peak": 100.0 * tf_dense / peaks["bf16_tflops"],
+            "pct_dense_bf16_peak_sustained": 100.0 * tf_dense / peaks["bf16_tflops_sustained"],
+            "peak_source": peak_src,
+            "aggregate_calls_per_s": world * 1e3 / ms,
+            "gpu_launches": args.steps * ns.launches_per_call(5),
+            "launches_per_step": ns.launches_per_call(5),
+            "wall_s_timed": wall,
+            "device_error_word": dev_err,
+            "roofline": roofline,
+            "breakdown": breakdown,
+            "clocks": clocks,
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+                    "steps": ne, "api": "newton_schulz_07_gb300.muon_ns -> muon_ns_ws (C ABI)"},
+            "parity": parity,
+            "cpu_baseline": cpu,
+            "per_shape": per_shape,
+            "kernel_source_hash": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_workload(torch, ns, w, dev, peaks, steps=10, warmup=3):
+    bits = ns_inputs.stack_bits(w)
+    G = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty_like(G)
+    ws = ns.alloc_workspace(w.batch, w.rows, w.cols, device=dev)
+    scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        ns.muon_ns(G, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    tot = 0.0
+    for i in range(steps):
+        scrub.fill_(i & 0xFF)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        ns.muon_ns(G, out=out, workspace=ws)
+        e.record(stream)
+        torch.cuda.synchronize()
+        tot += s.elapsed_time(e)
+    ms = tot / steps
+    tf = w.dense_flops() / (ms * 1e-3) / 1e12
+    res = {"ms": ms, "tflops_dense_equiv": tf, "tflops_useful": w.useful_flops() / (ms * 1e-3) / 1e12,
+           "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"], "batch": w.batch, "rows": w.rows,
+           "cols": w.cols, "steps": steps, "l2": "flushed between timed steps",
+           "device_error_word": ns.read_error(ws)}
+    if w.name in PAGES_H200_QUACK_MS:
+        res["pages_h200_quack_ms"] = PAGES_H200_QUACK_MS[w.name]
+    del G, out, ws, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    sys.exit(main())

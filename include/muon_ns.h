@@ -1,0 +1,199 @@
+/*
+ * muon_ns.h — C ABI of a GB300 (sm_103a) library for batched quintic
+ * Newton–Schulz (NS) orthogonalisation, the inner loop of the Muon optimizer
+ * step.
+ *
+ * What is computed (per matrix G of a stack, rows x cols, bf16 in and out):
+ *
+ *   X <- G / (||G||_F + eps)
+ *   if rows > cols: X <- X^T                       (internal m x n, m <= n)
+ *   repeat `steps` times:  A = X X^T;  B = b A + c A A;  X = a X + B X
+ *   if transposed: X <- X^T
+ *
+ * The three products are those of prime-rl PR #3873, Summary item 1
+ * ("Symmetric-GEMM Newton–Schulz": X·X^T, b·A + c·A·A, a·X + B·X, inside
+ * Dion's dense zeropower_via_newtonschulz5).  The leading axis of a stack is a
+ * batch of independent matrices (prime-rl PR #3873, Summary item 2;
+ * param-decomp PR #978 "stacked-NS Muon", What).  `steps` is the `ns_steps`
+ * setting of param-decomp PR #978 (default 5).  The default coefficients
+ * (a, b, c) = (3.4445, -4.7750, 2.0315), eps = 1e-7 and the transpose rule
+ * (transpose iff rows > cols) are the standard Muon quintic, which the pages
+ * name but do not print.
+ *
+ * Numerics: bf16 storage of X, A and B between steps; every product
+ * accumulates in fp32 on the tensor cores and every epilogue (b·A + c·(A A),
+ * a·X + B X) runs in fp32 and rounds once to bf16, as the fp32 alpha/beta
+ * epilogue of prime-rl PR #3873 (Results, note under the microbenchmark).
+ * A and B are stored bit-symmetric: one triangle is computed and mirrored
+ * (prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381 "Add
+ * --muon-use-syrk option", Summary).
+ *
+ * Conventions for every entry point below:
+ *   - Matrices are contiguous row-major stacks [batch][rows][cols] of raw
+ *     bf16 bit patterns (muon_bf16) in DEVICE memory owned by the caller.
+ *   - rows and cols must be multiples of 8 and every device pointer must be
+ *     16-byte aligned (16-byte rows for TMA; the same rule as prime-rl PR
+ *     #3873, Summary item 1, "dimension not divisible by 8").  This is an
+ *     error (MUON_NS_ERR_ALIGNMENT), never a silent fallback (Megatron-LM PR
+ *     #6381, "Version compatibility": a hard failure instead of a fallback).
+ *   - batch == 0, rows == 0 or cols == 0 is an empty problem: MUON_NS_OK,
+ *     nothing is launched and pointers may be NULL.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and the call
+ *     returns without synchronising.  Arguments are validated on the host
+ *     before anything is launched; a non-OK status means nothing was enqueued
+ *     (except MUON_NS_ERR_CUDA, which reports a failed launch).
+ *   - Only GPUs of compute capability 10.3 (sm_103) are supported; others get
+ *     MUON_NS_ERR_UNSUPPORTED_DEVICE.
+ *   - Limits: batch, rows, cols <= 1<<20 and each matrix below 2^31 elements.
+ *   - Errors found on the device (a bounded wait inside a kernel that ran out)
+ *     set a device error word; the call that launched the kernels cannot
+ *     see it, muon_ns_read_error() / muon_ns_cached_error() can.
+ */
+#ifndef MUON_NS_H
+#define MUON_NS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t muon_bf16; /* raw bfloat16 bit pattern */
+
+/* Status codes returned by every entry point. */
+enum {
+  MUON_NS_OK = 0,
+  MUON_NS_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, steps < 0, bad eps, too large */
+  MUON_NS_ERR_ALIGNMENT = 2,          /* rows/cols not multiples of 8, or a pointer not 16-byte aligned */
+  MUON_NS_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  MUON_NS_ERR_WORKSPACE = 4,          /* workspace NULL/too small, or cache too small during graph capture */
+  MUON_NS_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+  MUON_NS_ERR_TIMEOUT = 6             /* a kernel's bounded wait ran out (reported through the error word) */
+};
+
+/* Bits of the device error word. */
+#define MUON_NS_DEVERR_WAIT_TIMEOUT 1
+
+/* Library version string, e.g. "0.1.0". */
+const char* muon_ns_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* muon_ns_status_string(int status);
+
+/* Returns MUON_NS_OK if `device` (or the current device when device < 0) is
+ * supported, else MUON_NS_ERR_UNSUPPORTED_DEVICE (or MUON_NS_ERR_CUDA). */
+int muon_ns_device_supported(int device);
+
+/* ---------------------------------------------------------------------------
+ * Whole NS call.
+ * ------------------------------------------------------------------------- */
+
+/* Workspace regions, for muon_ns_workspace_region(). */
+enum {
+  MUON_NS_WS_TOTAL = 0,   /* whole workspace (offset 0) */
+  MUON_NS_WS_ERROR = 1,   /* int32 device error word */
+  MUON_NS_WS_NORMS = 2,   /* fp32 [batch]: ||G_k||_F of the last call */
+  MUON_NS_WS_X = 3,       /* bf16 [batch][rows][cols]: ping-pong iterate */
+  MUON_NS_WS_GRAM = 4,    /* bf16 [batch][m][m]: A of the last step, m = min(rows, cols) */
+  MUON_NS_WS_POLY = 5     /* bf16 [batch][m][m]: B of the last step */
+};
+
+/* Size of the workspace muon_ns_ws() needs for this problem, in bytes.
+ * Returns MUON_NS_OK or MUON_NS_ERR_INVALID_ARG / MUON_NS_ERR_ALIGNMENT. */
+int muon_ns_workspace_size(int batch, int rows, int cols, size_t* bytes);
+
+/* Offset and size in bytes of one region of the workspace (layout above).
+ * Tests read A (MUON_NS_WS_GRAM) after a call with steps = 1 to check that it
+ * is bit-symmetric. */
+int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* offset, size_t* bytes);
+
+/* out = NS(G) for a stack of `batch` matrices of rows x cols.
+ *   G, out     device, bf16 [batch][rows][cols]; out == G is allowed (in-place);
+ *              otherwise the two must not overlap.
+ *   steps      >= 0; steps == 0 returns G / (||G||_F + eps).
+ *   coeffs     host pointer to (a, b, c); NULL selects (3.4445, -4.7750, 2.0315).
+ *   eps        >= 0 and finite.  With eps == 0 an all-zero matrix gives NaN (0/0),
+ *              as the definition does; with eps > 0 it gives zeros.
+ *   workspace  device, >= muon_ns_workspace_size() bytes, 256-byte aligned,
+ *              caller-owned.  Nothing is allocated and nothing synchronises,
+ *              so the call can be captured in a CUDA graph.
+ * Kernel launches per call: 2 + 3 * steps (norm, scale, then per step the
+ * Gram, polynomial and update kernels). */
+int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
+               const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* As muon_ns_ws() with a workspace cached by the library per device (grown
+ * with cudaMalloc when too small, never freed before exit).  Growing is
+ * refused with MUON_NS_ERR_WORKSPACE while `stream` is being captured. */
+int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
+            const float* coeffs, float eps, cudaStream_t stream);
+
+/* Synchronises `stream`, copies the device error word of `workspace` into
+ * *device_error (0 = none) and, if `clear` is nonzero, resets it.  Returns
+ * MUON_NS_ERR_TIMEOUT if the word is nonzero, else MUON_NS_OK or an error. */
+int muon_ns_read_error(const void* workspace, int* device_error, int clear, cudaStream_t stream);
+
+/* Same for the workspace cached by muon_ns() on `device` (synchronises the
+ * device).  *device_error = 0 if no cached workspace exists yet. */
+int muon_ns_cached_error(int device, int* device_error);
+
+/* ---------------------------------------------------------------------------
+ * The steps of the path, one kernel each (the same kernels muon_ns_ws runs).
+ * `device_error` is an optional device int32 that receives
+ * MUON_NS_DEVERR_WAIT_TIMEOUT if a bounded wait runs out (may be NULL).
+ * ------------------------------------------------------------------------- */
+
+/* X = bf16(G * (1 / (||G_k||_F + eps))) per matrix, in the input orientation,
+ * and norms[k] = ||G_k||_F (fp32, sum of squares accumulated in fp32 in a
+ * fixed order, so the result is the same for a matrix alone or in any stack).
+ * `workspace` as for muon_ns_ws (only its header and norm regions are used).
+ * X == G is allowed.  Two kernel launches. */
+int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols, float eps,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Gram matrix of the internal orientation, bf16 [batch][m][m], m = min(rows, cols):
+ *   rows <= cols:  A = X X^T        rows > cols:  A = X^T X
+ * Only lower-triangle tiles are computed; each value is written to (i, j) and
+ * (j, i), so A is bit-symmetric.  fp32 accumulation, one rounding to bf16. */
+int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
+                 int* device_error, cudaStream_t stream);
+
+/* B = b A + c (A A) for a bit-symmetric A, bf16 [batch][m][m].  A A is formed
+ * as A A^T (equal for a bit-symmetric A) over lower-triangle tiles; the
+ * epilogue reads A and computes in fp32; B is bit-symmetric.  B != A. */
+int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, float c,
+                 int* device_error, cudaStream_t stream);
+
+/* The update of the iterate, in the input orientation, with m = min(rows, cols):
+ *   rows <= cols:  Xn = a X + B X     (B is rows x rows)
+ *   rows >  cols:  Xn = a X + X B     (B is cols x cols; this is (a X^T + B X^T)^T
+ *                                      for the bit-symmetric B)
+ * fp32 epilogue reading X.  Xn must not overlap X or B. */
+int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int batch, int rows,
+                   int cols, float a, int* device_error, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-only helpers (no GPU needed).
+ * ------------------------------------------------------------------------- */
+
+/* Kernel launches made by one muon_ns_ws() call: 2 + 3 * steps. */
+int muon_ns_launches_per_call(int steps);
+
+/* Persistent tile scheduler of the tensor-core kernels.  kind 0 = lower
+ * triangle of an m x m output (M == N), kind 1 = full M x N output.  Tiles are
+ * 128 x 256.  muon_ns_tile_count() returns the number of tiles of a launch
+ * (-1 on bad arguments); muon_ns_tile_coords() maps a linear tile index to
+ * (matrix, row tile, column tile) exactly as the kernels do. */
+long long muon_ns_tile_count(int kind, int batch, int M, int N);
+int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* matrix,
+                        int* row_tile, int* col_tile);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_NS_H */

@@ -1,0 +1,22 @@
+"""Batched quintic Newton–Schulz orthogonalisation for GB300 (sm_103a).
+
+The compute path is the CUDA library libmuon_ns.so (C ABI in
+include/muon_ns.h); this package is its thin PyTorch binding.
+"""
+from ._lib import LIB_PATH, MuonNSError, lib  # noqa: F401
+from .ns import (  # noqa: F401
+    DEFAULT_COEFFS,
+    DEFAULT_EPS,
+    alloc_workspace,
+    launches_per_call,
+    muon_ns,
+    muon_ns_gram,
+    muon_ns_normalize,
+    muon_ns_poly,
+    muon_ns_update,
+    read_error,
+    workspace_region,
+    workspace_size,
+)
+
+__version__ = "0.1.0"

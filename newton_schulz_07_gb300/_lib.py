@@ -1,0 +1,82 @@
+"""ctypes loader for libmuon_ns.so (the C ABI declared in include/muon_ns.h).
+
+The library is built in-tree by newton_schulz_07_gb300.build; there is no
+fallback: if it is missing, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmuon_ns.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_ALIGNMENT = 2
+ERR_UNSUPPORTED_DEVICE = 3
+ERR_WORKSPACE = 4
+ERR_CUDA = 5
+ERR_TIMEOUT = 6
+
+WS_TOTAL, WS_ERROR, WS_NORMS, WS_X, WS_GRAM, WS_POLY = range(6)
+
+_c_int, _c_ll, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+_pf = ctypes.POINTER(ctypes.c_float)
+_pi = ctypes.POINTER(ctypes.c_int)
+_psz = ctypes.POINTER(ctypes.c_size_t)
+
+# name -> (restype, argtypes); the exported C ABI, in header order.
+SIGNATURES = {
+    "muon_ns_version": (ctypes.c_char_p, []),
+    "muon_ns_status_string": (ctypes.c_char_p, [_c_int]),
+    "muon_ns_device_supported": (_c_int, [_c_int]),
+    "muon_ns_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _psz]),
+    "muon_ns_workspace_region": (_c_int, [_c_int, _c_int, _c_int, _c_int, _psz, _psz]),
+    "muon_ns_ws": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
+    "muon_ns": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp]),
+    "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),
+    "muon_ns_cached_error": (_c_int, [_c_int, _pi]),
+    "muon_ns_normalize": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp]),
+    "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "muon_ns_poly": (_c_int, [_vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
+    "muon_ns_update": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _vp]),
+    "muon_ns_launches_per_call": (_c_int, [_c_int]),
+    "muon_ns_tile_count": (_c_ll, [_c_int, _c_int, _c_int, _c_int]),
+    "muon_ns_tile_coords": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_ll, _pi, _pi, _pi]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MuonNSError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().muon_ns_status_string(status).decode()
+        super().__init__(f"{where}: status {status} ({msg})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loads it on first use; raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m newton_schulz_07_gb300.build` "
+                    "(there is no fallback implementation)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def check(status: int, where: str) -> None:
+    if status != OK:
+        raise MuonNSError(status, where)

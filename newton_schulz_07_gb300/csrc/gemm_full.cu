@@ -1,0 +1,17 @@
+// Instantiations of the tensor-core kernel for the update products
+// (a X + B X, and a Y + Y B for inputs kept in their tall orientation).
+#include "gemm_launch.cuh"
+
+namespace mns {
+
+cudaError_t launch_full_kmn(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                            int grid, cudaStream_t stream) {
+  return launch_tc_gemm<false, true, false>(a, b, args, grid, stream);
+}
+
+cudaError_t launch_full_kk(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                           int grid, cudaStream_t stream) {
+  return launch_tc_gemm<false, false, false>(a, b, args, grid, stream);
+}
+
+}  // namespace mns

@@ -1,0 +1,17 @@
+// Instantiations of the tensor-core kernel for the symmetric products
+// (Gram X X^T or Y^T Y, and b A + c A A).
+#include "gemm_launch.cuh"
+
+namespace mns {
+
+cudaError_t launch_sym_kk(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                          int grid, cudaStream_t stream) {
+  return launch_tc_gemm<false, false, true>(a, b, args, grid, stream);
+}
+
+cudaError_t launch_sym_mnmn(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                            int grid, cudaStream_t stream) {
+  return launch_tc_gemm<true, true, true>(a, b, args, grid, stream);
+}
+
+}  // namespace mns

@@ -1,0 +1,381 @@
+// Tensor-core product kernel shared by the three NS products.
+//
+//   out[i, j] = alpha * sum_k Aop[i, k] * Bop[k, j] + beta * addend[i, j]
+//
+// bf16 operands staged by TMA into 128-byte-swizzled shared memory, fp32
+// accumulation in TMEM by tcgen05.mma (M = 128, N = 256, K = 16 per
+// instruction), fp32 epilogue, one rounding to bf16.
+//
+// Template parameters:
+//   A_MN  the A operand is stored MN-major ([k][i], i contiguous) instead of
+//         K-major ([i][k], k contiguous);
+//   B_MN  the same for B ([k][j] instead of [j][k]);
+//   SYM   the output is symmetric: only lower-triangle tiles are scheduled and
+//         every value with j <= i is written to (i, j) and to (j, i), so the
+//         stored matrix is bit-symmetric (one triangle computed and mirrored,
+//         prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381, Summary).
+//
+// Uses (m <= n internally; Y = the tall input kept in its own orientation):
+//   Gram X X^T       <false, false, true>   both operands = rows of X
+//   Gram Y^T Y       <true,  true,  true>   both operands = columns of Y
+//   b A + c A A      <false, false, true>   A A = A A^T for a bit-symmetric A
+//   a X + B X        <false, true,  false>  X read MN-major
+//   a Y + Y B        <false, false, false>  B = B^T bitwise
+//
+// Roles (192 threads, one CTA per SM, persistent over the tile space):
+//   warp 0 lane 0   TMA producer: fills a kStages-deep ring of operand stages
+//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma per stage into one of two
+//                   256-column TMEM accumulators, commits release the stage
+//   warps 2..5      epilogue: tcgen05.ld of their 32-lane quarter, fp32
+//                   epilogue, bf16 stores; then free the accumulator
+// The double-buffered accumulator lets the epilogue of tile t overlap the
+// main loop of tile t + 1.
+//
+// Every wait on an mbarrier is bounded (clock64 budget).  When one runs out
+// the kernel records MUON_NS_DEVERR_WAIT_TIMEOUT in the error word, every role
+// leaves its loop, the producer waits (bounded) for its copies in flight, the
+// MMA issuer waits (bounded) for its MMAs, and TMEM is freed before return.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace mns {
+
+constexpr int kBlockK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
+constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kMnChunk = 64;                   // MN elements per 128-byte row
+constexpr int kMnChunkBytes = kMnChunk * kBlockK * 2;  // 8 KB
+
+struct GemmArgs {
+  TileSpace space;
+  int M, N, K;        // output rows, output columns, contraction length
+  int num_kb;         // ceil(K / kBlockK)
+  uint16_t* out;      // bf16 [batch][M][N], row stride ld
+  const uint16_t* addend;  // same layout, or nullptr
+  long long ld;
+  long long bstride;
+  float alpha, beta;
+  int* err;           // device error word, or nullptr
+  long long budget;   // clock64 cycles per wait
+};
+
+namespace detail {
+
+struct Sync {
+  uint32_t full[kStages];
+  uint32_t empty[kStages];
+  uint32_t tfull[2];
+  uint32_t tempty[2];
+  uint32_t mma_done;
+};
+
+__device__ __forceinline__ void raise_error(volatile int* abort_flag, int* err) {
+  *abort_flag = 1;
+  if (err) atomicOr(err, 1);
+}
+
+// Bounded wait.  Returns false (and raises the abort flag on expiry) if the
+// phase did not complete within the budget or another role aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int* err,
+                                             long long budget) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > budget) {
+      raise_error(abort_flag, err);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used on the way out: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > budget) return;
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+}  // namespace detail
+
+template <bool A_MN, bool B_MN, bool SYM>
+__global__ void __launch_bounds__(kThreads, 1)
+    ns_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &abort_sh;
+
+  const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  detail::Sync sy;
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) {
+    sy.full[s] = ptx::smem_u32(&bars[s]);
+    sy.empty[s] = ptx::smem_u32(&bars[kStages + s]);
+  }
+  sy.tfull[0] = ptx::smem_u32(&bars[2 * kStages + 0]);
+  sy.tfull[1] = ptx::smem_u32(&bars[2 * kStages + 1]);
+  sy.tempty[0] = ptx::smem_u32(&bars[2 * kStages + 2]);
+  sy.tempty[1] = ptx::smem_u32(&bars[2 * kStages + 3]);
+  sy.mma_done = ptx::smem_u32(&bars[2 * kStages + 4]);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(sy.full[s], 1);
+      ptx::mbar_init(sy.empty[s], 1);
+    }
+    ptx::mbar_init(sy.tfull[0], 1);
+    ptx::mbar_init(sy.tfull[1], 1);
+    ptx::mbar_init(sy.tempty[0], kEpiThreads);
+    ptx::mbar_init(sy.tempty[1], kEpiThreads);
+    ptx::mbar_init(sy.mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  const TileSpace& sp = args.space;
+  const int num_kb = args.num_kb;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0;   // stages with a load issued at least once
+      uint32_t issued_phase = 0;  // parity of the last load issued per stage
+      for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+        int b, I, J;
+        tile_decode(sp, t, &b, &I, &J);
+        const int row0 = I * kTileM;
+        const int col0 = J * kTileN;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!detail::wait_bounded(sy.empty[stage], phase ^ 1u, abort_flag, args.err,
+                                    args.budget)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(sy.full[stage], kStageBytes);
+          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sb = sa + kABytes;
+          const int k0 = kb * kBlockK;
+          if (A_MN) {
+#pragma unroll
+            for (int c = 0; c < kTileM / kMnChunk; ++c)
+              ptx::tma_load_3d(sa + c * kMnChunkBytes, &tmA, sy.full[stage], row0 + c * kMnChunk,
+                               k0, b);
+          } else {
+            ptx::tma_load_3d(sa, &tmA, sy.full[stage], k0, row0, b);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int c = 0; c < kTileN / kMnChunk; ++c)
+              ptx::tma_load_3d(sb + c * kMnChunkBytes, &tmB, sy.full[stage], col0 + c * kMnChunk,
+                               k0, b);
+          } else {
+            ptx::tma_load_3d(sb, &tmB, sy.full[stage], k0, col0, b);
+          }
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Wait for every copy still in flight before the CTA can exit.
+#pragma unroll
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) detail::drain_wait(sy.full[s], (issued_phase >> s) & 1u, args.budget);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t tphase = 0;
+      for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+        if (!detail::wait_bounded(sy.tempty[buf], tphase ^ 1u, abort_flag, args.err, args.budget))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!detail::wait_bounded(sy.full[stage], phase, abort_flag, args.err, args.budget)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            const uint64_t ad = A_MN ? ptx::sw128_desc(sa + kk * 2048, kMnChunkBytes, 1024)
+                                     : ptx::sw128_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::sw128_desc(sb + kk * 2048, kMnChunkBytes, 1024)
+                                     : ptx::sw128_desc(sb + kk * 32, 16, 1024);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(sy.empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(sy.tfull[buf]);
+        buf ^= 1;
+        if (buf == 0) tphase ^= 1u;
+      }
+      // Every MMA issued by this thread has finished once this arrives.
+      ptx::mma_commit(sy.mma_done);
+      detail::drain_wait(sy.mma_done, 0, args.budget);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int buf = 0;
+    uint32_t tphase = 0;
+    for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+      int b, I, J;
+      tile_decode(sp, t, &b, &I, &J);
+      int ready = 0;
+      if (lane == 0)
+        ready = detail::wait_bounded(sy.tfull[buf], tphase, abort_flag, args.err, args.budget) ? 1 : 0;
+      ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+      if (!ready) break;
+      __syncwarp();
+      ptx::tc_fence_after();
+
+      const long long gi = static_cast<long long>(I) * kTileM + r_in_tile;
+      const int warp_row_max = I * kTileM + q * 32 + 31;
+      const bool row_ok = gi < args.M;
+      uint16_t* outm = args.out + static_cast<long long>(b) * args.bstride;
+      const uint16_t* addm =
+          args.addend ? args.addend + static_cast<long long>(b) * args.bstride : nullptr;
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                              static_cast<uint32_t>(buf * kTileN);
+
+#pragma unroll 1
+      for (int c = 0; c < kTileN / 32; ++c) {
+        const int gj0 = J * kTileN + c * 32;
+        if (gj0 >= args.N) break;                   // warp-uniform
+        if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
+        uint32_t v[32];
+        ptx::tmem_ld_32cols(t_lane + c * 32, v);
+        ptx::tmem_wait_ld();
+        if (!row_ok) continue;
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
+        if (addm != nullptr) {
+          const uint4* src = reinterpret_cast<const uint4*>(addm + gi * args.ld + gj0);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (gj0 + 8 * g + 8 <= args.N) {
+              const uint4 w = __ldg(src + g);
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                f[8 * g + 2 * h] = fmaf(args.beta, detail::bf16_lo(ws[h]), f[8 * g + 2 * h]);
+                f[8 * g + 2 * h + 1] = fmaf(args.beta, detail::bf16_hi(ws[h]), f[8 * g + 2 * h + 1]);
+              }
+            }
+          }
+        }
+        uint32_t hv[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
+        uint16_t* rowp = outm + gi * args.ld + gj0;
+        if (!SYM) {
+          uint4* dst = reinterpret_cast<uint4*>(rowp);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (gj0 + 8 * g + 8 <= args.N)
+              dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
+        } else {
+          if (gj0 + 31 <= gi && gj0 + 32 <= args.N) {
+            uint4* dst = reinterpret_cast<uint4*>(rowp);
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const long long gj = gj0 + j;
+              if (gj <= gi && gj < args.N)
+                rowp[j] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+            }
+          }
+          // Mirror: (gj, gi) for gj < gi.  Lanes hold consecutive gi, so each
+          // store instruction writes 64 contiguous bytes of row gj.
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const long long gj = gj0 + j;
+            if (gj < gi && gj < args.N)
+              outm[gj * args.ld + gi] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sy.tempty[buf]);
+      buf ^= 1;
+      if (buf == 0) tphase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace mns

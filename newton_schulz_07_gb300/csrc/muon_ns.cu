@@ -1,0 +1,545 @@
+// C-ABI entry points (include/muon_ns.h): argument checks, workspace layout,
+// TMA tensor maps and the launch sequence of one batched NS call.
+//
+//   norm (ns_norm_partial) -> scale (ns_scale) -> steps x [Gram, poly, update]
+//
+// Tall inputs (rows > cols) are never transposed in memory: with Y = X^T kept
+// in the input's orientation, A = Y^T Y reads Y MN-major, and the update
+// Y' = a Y + Y B reads B K-major (B is bit-symmetric), so the result lands in
+// the input orientation directly.
+//
+// The iterate ping-pongs between the workspace and `out`, starting where the
+// parity of `steps` makes the last step write `out`; there is no final copy.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "muon_ns.h"
+#include "gemm_tc.cuh"
+#include "internal.h"
+#include "norm.cuh"
+
+namespace {
+
+using mns::GemmArgs;
+
+constexpr long long kMaxDim = 1 << 20;
+constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr long long kWaitBudgetCycles = 4000000000LL;  // about 2 s at 2 GHz
+
+struct Problem {
+  long long batch, R, C, m, n;
+  bool T;  // rows > cols: the input is kept tall (Y = X^T)
+};
+
+struct Layout {
+  size_t error, tickets, partials, norms, x, a, b, total;
+  size_t x_bytes, a_bytes;
+  int chunks;
+};
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int check_shape(long long batch, long long rows, long long cols, Problem* p, bool* empty) {
+  if (batch < 0 || rows < 0 || cols < 0) return MUON_NS_ERR_INVALID_ARG;
+  if (batch > kMaxDim || rows > kMaxDim || cols > kMaxDim) return MUON_NS_ERR_INVALID_ARG;
+  if (rows * cols >= (1LL << 31)) return MUON_NS_ERR_INVALID_ARG;
+  if (rows % 8 != 0 || cols % 8 != 0) return MUON_NS_ERR_ALIGNMENT;
+  p->batch = batch;
+  p->R = rows;
+  p->C = cols;
+  p->T = rows > cols;
+  p->m = p->T ? cols : rows;
+  p->n = p->T ? rows : cols;
+  *empty = batch == 0 || rows == 0 || cols == 0;
+  return MUON_NS_OK;
+}
+
+Layout make_layout(const Problem& p) {
+  Layout L;
+  const long long vec = p.R * p.C / 8;
+  L.chunks = static_cast<int>((vec + mns::kNormChunkVec - 1) / mns::kNormChunkVec);
+  if (L.chunks < 1) L.chunks = 1;
+  size_t off = 0;
+  L.error = off;
+  off += 256;
+  L.tickets = off;
+  off = round_up(off + 4 * static_cast<size_t>(p.batch), 256);
+  L.partials = off;
+  off = round_up(off + 4 * static_cast<size_t>(p.batch) * L.chunks, 256);
+  L.norms = off;
+  off = round_up(off + 4 * static_cast<size_t>(p.batch), 1024);
+  L.x = off;
+  L.x_bytes = 2 * static_cast<size_t>(p.batch) * p.R * p.C;
+  off = round_up(off + L.x_bytes, 1024);
+  L.a = off;
+  L.a_bytes = 2 * static_cast<size_t>(p.batch) * p.m * p.m;
+  off = round_up(off + L.a_bytes, 1024);
+  L.b = off;
+  off = round_up(off + L.a_bytes, 1024);
+  L.total = off;
+  return L;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------- devices --
+
+struct DevInfo {
+  int checked;
+  int status;
+  int sms;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+int current_device_info(DevInfo* out, int* dev_out = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (dev < 0 || dev >= 64) return MUON_NS_ERR_UNSUPPORTED_DEVICE;
+  if (dev_out) *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MUON_NS_ERR_CUDA;
+    }
+    d.status = (major == 10 && minor == 3) ? MUON_NS_OK : MUON_NS_ERR_UNSUPPORTED_DEVICE;
+    d.sms = sms;
+    d.checked = 1;
+  }
+  *out = d;
+  return d.status;
+}
+
+// ------------------------------------------------------------- tensor maps --
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 3-D bf16 map over a stack [batch][rows][inner] (inner contiguous) with a
+// box of box_inner x box_rows x 1 and 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, long long inner, long long rows,
+              long long batch, int box_inner, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 2),
+                           static_cast<cuuint64_t>(inner * rows * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- launches --
+
+GemmArgs base_args(int sym, long long batch, long long M, long long N, long long K, int* err) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
+                                 static_cast<int>(N));
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.num_kb = static_cast<int>((K + mns::kBlockK - 1) / mns::kBlockK);
+  a.ld = N;
+  a.bstride = M * N;
+  a.alpha = 1.0f;
+  a.beta = 0.0f;
+  a.err = err;
+  a.budget = kWaitBudgetCycles;
+  return a;
+}
+
+int grid_for(const GemmArgs& a, int sms) {
+  const long long g = a.space.total < sms ? a.space.total : sms;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? MUON_NS_OK : MUON_NS_ERR_CUDA; }
+
+int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, int* err, int sms,
+             cudaStream_t st) {
+  CUtensorMap ta, tb;
+  GemmArgs a = base_args(1, p.batch, p.m, p.m, p.n, err);
+  a.out = A;
+  if (!p.T) {
+    // X [batch][m][n]: rows of X are the K-major operand rows.
+    if (!make_map(&ta, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
+        !make_map(&tb, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileN))
+      return MUON_NS_ERR_CUDA;
+    return to_status(mns::launch_sym_kk(ta, tb, a, grid_for(a, sms), st));
+  }
+  // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
+  if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kMnChunk, mns::kBlockK)) return MUON_NS_ERR_CUDA;
+  return to_status(mns::launch_sym_mnmn(ta, ta, a, grid_for(a, sms), st));
+}
+
+int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float b, float c,
+             int* err, int sms, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, m, m, batch, mns::kBlockK, mns::kTileM) ||
+      !make_map(&tb, A, m, m, batch, mns::kBlockK, mns::kTileN))
+    return MUON_NS_ERR_CUDA;
+  GemmArgs a = base_args(1, batch, m, m, m, err);
+  a.out = B;
+  a.addend = A;
+  a.alpha = c;
+  a.beta = b;
+  return to_status(mns::launch_sym_kk(ta, tb, a, grid_for(a, sms), st));
+}
+
+int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, uint16_t* Xn, float alpha_x,
+               int* err, int sms, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!p.T) {
+    // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
+    if (!make_map(&ta, B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
+        !make_map(&tb, X, p.n, p.m, p.batch, mns::kMnChunk, mns::kBlockK))
+      return MUON_NS_ERR_CUDA;
+    GemmArgs a = base_args(0, p.batch, p.m, p.n, p.m, err);
+    a.out = Xn;
+    a.addend = X;
+    a.beta = alpha_x;
+    return to_status(mns::launch_full_kmn(ta, tb, a, grid_for(a, sms), st));
+  }
+  // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
+  if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kBlockK, mns::kTileM) ||
+      !make_map(&tb, B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileN))
+    return MUON_NS_ERR_CUDA;
+  GemmArgs a = base_args(0, p.batch, p.n, p.m, p.m, err);
+  a.out = Xn;
+  a.addend = X;
+  a.beta = alpha_x;
+  return to_status(mns::launch_full_kk(ta, tb, a, grid_for(a, sms), st));
+}
+
+int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* X, float eps,
+                  uint8_t* ws, cudaStream_t st) {
+  const long long vec = p.R * p.C / 8;
+  if (cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
+  mns::ns_norm_partial<<<grid, mns::kNormThreads, 0, st>>>(
+      reinterpret_cast<const uint4*>(G), vec, L.chunks, reinterpret_cast<float*>(ws + L.partials),
+      reinterpret_cast<unsigned int*>(ws + L.tickets), reinterpret_cast<float*>(ws + L.norms));
+  if (cudaGetLastError() != cudaSuccess) return MUON_NS_ERR_CUDA;
+  mns::ns_scale<<<grid, mns::kNormThreads, 0, st>>>(reinterpret_cast<const uint4*>(G),
+                                                    reinterpret_cast<uint4*>(X), vec,
+                                                    reinterpret_cast<const float*>(ws + L.norms),
+                                                    eps);
+  return cudaGetLastError() == cudaSuccess ? MUON_NS_OK : MUON_NS_ERR_CUDA;
+}
+
+int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, int steps,
+           const float abc[3], float eps, uint8_t* ws, int sms, cudaStream_t st) {
+  int* err = reinterpret_cast<int*>(ws + L.error);
+  if (cudaMemsetAsync(ws + L.error, 0, 256, st) != cudaSuccess) return MUON_NS_ERR_CUDA;
+  uint16_t* wsx = reinterpret_cast<uint16_t*>(ws + L.x);
+  uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
+  uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
+  uint16_t* cur = (steps % 2 == 1) ? wsx : out;
+  int s = run_normalize(p, L, G, cur, eps, ws, st);
+  if (s != MUON_NS_OK) return s;
+  for (int k = 0; k < steps; ++k) {
+    uint16_t* nxt = (cur == out) ? wsx : out;
+    if ((s = run_gram(p, cur, A, err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_poly(p.batch, p.m, A, B, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_update(p, cur, B, nxt, abc[0], err, sms, st)) != MUON_NS_OK) return s;
+    cur = nxt;
+  }
+  return MUON_NS_OK;
+}
+
+int check_scalars(int steps, const float* coeffs, float eps, float abc[3]) {
+  if (steps < 0) return MUON_NS_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MUON_NS_ERR_INVALID_ARG;
+  const float* c = coeffs ? coeffs : kDefaultCoeffs;
+  for (int i = 0; i < 3; ++i) {
+    if (!std::isfinite(c[i])) return MUON_NS_ERR_INVALID_ARG;
+    abc[i] = c[i];
+  }
+  return MUON_NS_OK;
+}
+
+// ----------------------------------------------------- cached workspaces --
+
+struct Cache {
+  void* ptr;
+  size_t bytes;
+};
+std::mutex g_cache_mu;
+Cache g_cache[64];
+
+}  // namespace
+
+extern "C" {
+
+const char* muon_ns_version(void) { return "0.1.0"; }
+
+const char* muon_ns_status_string(int status) {
+  switch (status) {
+    case MUON_NS_OK: return "ok";
+    case MUON_NS_ERR_INVALID_ARG: return "invalid argument";
+    case MUON_NS_ERR_ALIGNMENT: return "alignment: rows/cols must be multiples of 8 and pointers 16-byte aligned";
+    case MUON_NS_ERR_UNSUPPORTED_DEVICE: return "unsupported device: compute capability 10.3 (sm_103) required";
+    case MUON_NS_ERR_WORKSPACE: return "workspace missing or too small";
+    case MUON_NS_ERR_CUDA: return "CUDA call failed";
+    case MUON_NS_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int muon_ns_device_supported(int device) {
+  int prev = -1;
+  if (device >= 0) {
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+      cudaGetLastError();
+      return MUON_NS_ERR_UNSUPPORTED_DEVICE;
+    }
+  }
+  DevInfo d;
+  const int s = current_device_info(&d);
+  if (prev >= 0 && prev != device) cudaSetDevice(prev);
+  return s;
+}
+
+int muon_ns_workspace_size(int batch, int rows, int cols, size_t* bytes) {
+  if (!bytes) return MUON_NS_ERR_INVALID_ARG;
+  Problem p;
+  bool empty;
+  const int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  *bytes = empty ? 0 : make_layout(p).total;
+  return MUON_NS_OK;
+}
+
+int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* offset,
+                             size_t* bytes) {
+  if (!offset || !bytes) return MUON_NS_ERR_INVALID_ARG;
+  Problem p;
+  bool empty;
+  const int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  const Layout L = make_layout(p);
+  switch (region) {
+    case MUON_NS_WS_TOTAL: *offset = 0; *bytes = L.total; break;
+    case MUON_NS_WS_ERROR: *offset = L.error; *bytes = 4; break;
+    case MUON_NS_WS_NORMS: *offset = L.norms; *bytes = 4 * static_cast<size_t>(p.batch); break;
+    case MUON_NS_WS_X: *offset = L.x; *bytes = L.x_bytes; break;
+    case MUON_NS_WS_GRAM: *offset = L.a; *bytes = L.a_bytes; break;
+    case MUON_NS_WS_POLY: *offset = L.b; *bytes = L.a_bytes; break;
+    default: return MUON_NS_ERR_INVALID_ARG;
+  }
+  return MUON_NS_OK;
+}
+
+int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
+               const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  float abc[3];
+  if ((s = check_scalars(steps, coeffs, eps, abc)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!G || !out) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(out)) return MUON_NS_ERR_ALIGNMENT;
+  const Layout L = make_layout(p);
+  if (!workspace || workspace_bytes < L.total) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_ns(p, L, G, out, steps, abc, eps, static_cast<uint8_t*>(workspace), d.sms, stream);
+}
+
+int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
+            const float* coeffs, float eps, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  float abc[3];
+  if ((s = check_scalars(steps, coeffs, eps, abc)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!G || !out) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(out)) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  int dev = 0;
+  if ((s = current_device_info(&d, &dev)) != MUON_NS_OK) return s;
+  const Layout L = make_layout(p);
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  Cache& c = g_cache[dev];
+  if (c.bytes < L.total) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return MUON_NS_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return MUON_NS_ERR_WORKSPACE;
+    if (c.ptr) {
+      cudaFree(c.ptr);
+      c.ptr = nullptr;
+      c.bytes = 0;
+    }
+    if (cudaMalloc(&c.ptr, L.total) != cudaSuccess) {
+      cudaGetLastError();
+      c.ptr = nullptr;
+      return MUON_NS_ERR_CUDA;
+    }
+    c.bytes = L.total;
+  }
+  return run_ns(p, L, G, out, steps, abc, eps, static_cast<uint8_t*>(c.ptr), d.sms, stream);
+}
+
+int muon_ns_read_error(const void* workspace, int* device_error, int clear, cudaStream_t stream) {
+  if (!workspace || !device_error) return MUON_NS_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  if (clear && v != 0 &&
+      cudaMemset(const_cast<void*>(workspace), 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  *device_error = v;
+  return v ? MUON_NS_ERR_TIMEOUT : MUON_NS_OK;
+}
+
+int muon_ns_cached_error(int device, int* device_error) {
+  if (!device_error || device < 0 || device >= 64) return MUON_NS_ERR_INVALID_ARG;
+  void* ptr;
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    ptr = g_cache[device].ptr;
+  }
+  *device_error = 0;
+  if (!ptr) return MUON_NS_OK;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  const int s = muon_ns_read_error(ptr, device_error, 0, nullptr);
+  cudaSetDevice(prev);
+  return s;
+}
+
+int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols, float eps,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MUON_NS_ERR_INVALID_ARG;
+  if (empty) return MUON_NS_OK;
+  if (!G || !X) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(X)) return MUON_NS_ERR_ALIGNMENT;
+  const Layout L = make_layout(p);
+  if (!workspace || workspace_bytes < L.total) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_normalize(p, L, G, X, eps, static_cast<uint8_t*>(workspace), stream);
+}
+
+int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
+                 int* device_error, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!X || !A) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(A)) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_gram(p, X, A, device_error, d.sms, stream);
+}
+
+int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, float c,
+                 int* device_error, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, m, m, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (!std::isfinite(b) || !std::isfinite(c)) return MUON_NS_ERR_INVALID_ARG;
+  if (empty) return MUON_NS_OK;
+  if (!A || !B || A == B) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B)) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_poly(p.batch, p.m, A, B, b, c, device_error, d.sms, stream);
+}
+
+int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int batch, int rows,
+                   int cols, float a, int* device_error, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (!std::isfinite(a)) return MUON_NS_ERR_INVALID_ARG;
+  if (empty) return MUON_NS_OK;
+  if (!X || !B || !Xn || Xn == X || Xn == B) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(B) || !aligned16(Xn)) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_update(p, X, B, Xn, a, device_error, d.sms, stream);
+}
+
+int muon_ns_launches_per_call(int steps) { return steps < 0 ? -1 : 2 + 3 * steps; }
+
+long long muon_ns_tile_count(int kind, int batch, int M, int N) {
+  if ((kind != 0 && kind != 1) || batch < 0 || M < 0 || N < 0) return -1;
+  if (kind == 0 && M != N) return -1;
+  return mns::make_tile_space(kind == 0 ? 1 : 0, batch, M, N).total;
+}
+
+int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* matrix,
+                        int* row_tile, int* col_tile) {
+  if (!matrix || !row_tile || !col_tile) return MUON_NS_ERR_INVALID_ARG;
+  const long long total = muon_ns_tile_count(kind, batch, M, N);
+  if (total < 0 || tile < 0 || tile >= total) return MUON_NS_ERR_INVALID_ARG;
+  const mns::TileSpace sp = mns::make_tile_space(kind == 0 ? 1 : 0, batch, M, N);
+  mns::tile_decode(sp, tile, matrix, row_tile, col_tile);
+  return MUON_NS_OK;
+}
+
+}  // extern "C"

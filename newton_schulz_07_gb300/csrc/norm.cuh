@@ -1,0 +1,132 @@
+// Frobenius norm and scale: the first step of NS, X = G / (||G||_F + eps).
+//
+// Two memory-bound kernels over a stack of matrices stored as 16-byte vectors
+// of 8 bf16 values (rows and columns are multiples of 8, so every matrix
+// starts on a 16-byte boundary):
+//
+//   ns_norm_partial  grid (chunks, batch): each CTA sums the squares of one
+//                    chunk of kNormChunkVec vectors in fp32 (per thread, then a
+//                    fixed xor-shuffle tree per warp, then the warps in order)
+//                    and stores the partial.  The CTA that takes the last
+//                    ticket of its matrix adds the partials in a fixed order
+//                    and writes ||G||_F.  The chunking depends only on the
+//                    matrix size, so a matrix gets bit-identical norms alone or
+//                    in any stack.
+//   ns_scale         grid (chunks, batch): X = bf16_rn(G * (1 / (nu + eps))),
+//                    elementwise in the input orientation (G may equal X).
+//
+// The norm is the per-matrix Frobenius normalisation of Dion's dense NS named
+// by prime-rl PR #3873, Summary item 1.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+namespace mns {
+
+constexpr int kNormThreads = 256;
+constexpr int kNormVecPerThread = 8;
+constexpr long long kNormChunkVec = static_cast<long long>(kNormThreads) * kNormVecPerThread;
+
+namespace detail {
+
+__device__ __forceinline__ float sumsq_bf16x8(const uint4 w) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  float s = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float lo = __uint_as_float(ws[h] << 16);
+    const float hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+    s = fmaf(lo, lo, s);
+    s = fmaf(hi, hi, s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  float total = 0.0f;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) total += red[w];
+  }
+  __syncthreads();
+  return total;  // valid in thread 0
+}
+
+}  // namespace detail
+
+__global__ void __launch_bounds__(kNormThreads)
+    ns_norm_partial(const uint4* __restrict__ G, long long vec_per_matrix, int chunks,
+                    float* __restrict__ partials, unsigned int* __restrict__ tickets,
+                    float* __restrict__ norms) {
+  __shared__ float red[kNormThreads / 32];
+  __shared__ int is_last;
+  const int b = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const uint4* g = G + static_cast<long long>(b) * vec_per_matrix;
+  const long long base = static_cast<long long>(chunk) * kNormChunkVec;
+
+  uint4 w[kNormVecPerThread];
+#pragma unroll
+  for (int it = 0; it < kNormVecPerThread; ++it) {
+    const long long i = base + it * kNormThreads + threadIdx.x;
+    w[it] = i < vec_per_matrix ? __ldcs(g + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int it = 0; it < kNormVecPerThread; ++it) acc += detail::sumsq_bf16x8(w[it]);
+
+  const float part = detail::block_sum_fixed(acc, red);
+  if (threadIdx.x == 0) {
+    partials[static_cast<long long>(b) * chunks + chunk] = part;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&tickets[b], 1u);
+    is_last = (ticket == static_cast<unsigned int>(chunks - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  float s = 0.0f;
+  for (int i = threadIdx.x; i < chunks; i += kNormThreads)
+    s += __ldcg(&partials[static_cast<long long>(b) * chunks + i]);
+  const float total = detail::block_sum_fixed(s, red);
+  if (threadIdx.x == 0) norms[b] = sqrtf(total);
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    ns_scale(const uint4* G, uint4* X, long long vec_per_matrix, const float* __restrict__ norms,
+             float eps) {
+  const int b = blockIdx.y;
+  const float s = 1.0f / (norms[b] + eps);
+  const uint4* g = G + static_cast<long long>(b) * vec_per_matrix;
+  uint4* x = X + static_cast<long long>(b) * vec_per_matrix;
+  const long long base = static_cast<long long>(blockIdx.x) * kNormChunkVec;
+  uint4 w[kNormVecPerThread];
+#pragma unroll
+  for (int it = 0; it < kNormVecPerThread; ++it) {
+    const long long i = base + it * kNormThreads + threadIdx.x;
+    w[it] = i < vec_per_matrix ? g[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int it = 0; it < kNormVecPerThread; ++it) {
+    const long long i = base + it * kNormThreads + threadIdx.x;
+    if (i >= vec_per_matrix) continue;
+    uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float lo = __uint_as_float(ws[h] << 16) * s;
+      const float hi = __uint_as_float(ws[h] & 0xFFFF0000u) * s;
+      ws[h] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    }
+    x[i] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  }
+}
+
+}  // namespace mns

@@ -1,0 +1,151 @@
+"""PyTorch-facing binding of the C ABI: argument marshalling only.
+
+Every step of the computation runs in the CUDA library; PyTorch supplies the
+device memory and the current stream.  Names follow the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+DEFAULT_COEFFS = (3.4445, -4.7750, 2.0315)
+DEFAULT_EPS = 1e-7
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _shape3(t):
+    if t.dim() == 2:
+        return 1, t.shape[0], t.shape[1]
+    if t.dim() == 3:
+        return t.shape[0], t.shape[1], t.shape[2]
+    raise ValueError(f"expected a 2-D matrix or a 3-D stack, got shape {tuple(t.shape)}")
+
+
+def _check_bf16(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(batch: int, rows: int, cols: int) -> int:
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_workspace_size(batch, rows, cols, ctypes.byref(n)), "muon_ns_workspace_size")
+    return n.value
+
+
+def workspace_region(batch: int, rows: int, cols: int, region: int) -> tuple[int, int]:
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_workspace_region(batch, rows, cols, region, ctypes.byref(off), ctypes.byref(nb)),
+               "muon_ns_workspace_region")
+    return off.value, nb.value
+
+
+def alloc_workspace(batch: int, rows: int, cols: int, device=None) -> torch.Tensor:
+    """A uint8 device buffer of muon_ns_workspace_size() bytes (256-byte aligned)."""
+    return torch.empty(max(workspace_size(batch, rows, cols), 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def _coeffs(coeffs):
+    a = (ctypes.c_float * 3)(*[float(v) for v in coeffs])
+    return ctypes.cast(a, ctypes.POINTER(ctypes.c_float))
+
+
+def muon_ns(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS,
+            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Batched quintic Newton–Schulz of a bf16 matrix or (batch, rows, cols) stack.
+
+    With `workspace` (from alloc_workspace) the call goes through muon_ns_ws;
+    otherwise through muon_ns and the library's cached workspace.  `out` may be G.
+    """
+    _check_bf16(G, "G")
+    b, r, c = _shape3(G)
+    if out is None:
+        out = torch.empty_like(G)
+    _check_bf16(out, "out")
+    if out.shape != G.shape or out.device != G.device:
+        raise ValueError("out must match G in shape and device")
+    L = _lib.lib()
+    cf = _coeffs(coeffs)
+    with torch.cuda.device(G.device):
+        st = _stream(G.device)
+        if workspace is not None:
+            if workspace.device != G.device:
+                raise ValueError("workspace must be on G's device")
+            s = L.muon_ns_ws(_ptr(G), _ptr(out), b, r, c, int(steps), cf, float(eps),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(), st)
+            _lib.check(s, "muon_ns_ws")
+        else:
+            _lib.check(L.muon_ns(_ptr(G), _ptr(out), b, r, c, int(steps), cf, float(eps), st), "muon_ns")
+    return out
+
+
+def muon_ns_normalize(G: torch.Tensor, workspace: torch.Tensor, eps: float = DEFAULT_EPS,
+                      X: torch.Tensor | None = None) -> torch.Tensor:
+    _check_bf16(G, "G")
+    b, r, c = _shape3(G)
+    X = torch.empty_like(G) if X is None else X
+    with torch.cuda.device(G.device):
+        _lib.check(_lib.lib().muon_ns_normalize(_ptr(G), _ptr(X), b, r, c, float(eps), _ptr(workspace),
+                                                workspace.numel(), _stream(G.device)), "muon_ns_normalize")
+    return X
+
+
+def muon_ns_gram(X: torch.Tensor, A: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+    _check_bf16(X, "X")
+    b, r, c = _shape3(X)
+    m = min(r, c)
+    if A is None:
+        A = torch.empty((b, m, m) if X.dim() == 3 else (m, m), dtype=torch.bfloat16, device=X.device)
+    with torch.cuda.device(X.device):
+        _lib.check(_lib.lib().muon_ns_gram(_ptr(X), _ptr(A), b, r, c, _ptr(device_error), _stream(X.device)),
+                   "muon_ns_gram")
+    return A
+
+
+def muon_ns_poly(A: torch.Tensor, b: float, c: float, B: torch.Tensor | None = None,
+                 device_error: torch.Tensor | None = None):
+    _check_bf16(A, "A")
+    bt, m, m2 = _shape3(A)
+    if m != m2:
+        raise ValueError("A must be square")
+    B = torch.empty_like(A) if B is None else B
+    with torch.cuda.device(A.device):
+        _lib.check(_lib.lib().muon_ns_poly(_ptr(A), _ptr(B), bt, m, float(b), float(c), _ptr(device_error),
+                                           _stream(A.device)), "muon_ns_poly")
+    return B
+
+
+def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor | None = None,
+                   device_error: torch.Tensor | None = None):
+    _check_bf16(X, "X")
+    _check_bf16(B, "B")
+    bt, r, c = _shape3(X)
+    Xn = torch.empty_like(X) if Xn is None else Xn
+    with torch.cuda.device(X.device):
+        _lib.check(_lib.lib().muon_ns_update(_ptr(X), _ptr(B), _ptr(Xn), bt, r, c, float(a), _ptr(device_error),
+                                             _stream(X.device)), "muon_ns_update")
+    return Xn
+
+
+def read_error(workspace: torch.Tensor, clear: bool = False) -> int:
+    v = ctypes.c_int(0)
+    with torch.cuda.device(workspace.device):
+        s = _lib.lib().muon_ns_read_error(_ptr(workspace), ctypes.byref(v), int(clear), _stream(workspace.device))
+    if s not in (_lib.OK, _lib.ERR_TIMEOUT):
+        _lib.check(s, "muon_ns_read_error")
+    return v.value
+
+
+def launches_per_call(steps: int) -> int:
+    return _lib.lib().muon_ns_launches_per_call(steps)

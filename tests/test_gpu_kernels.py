@@ -1,0 +1,104 @@
+"""Per-kernel GPU parity through the C ABI: each kernel of the path against the
+oracle's definition of its step, evaluated in fp64 on the same bf16 inputs.
+
+Tolerance, from the arithmetic: each kernel rounds its fp32 result to bf16
+once (relative error <= 2^-9 per element, so <= 2^-9 ~ 1.95e-3 in relative
+Frobenius norm) after an fp32 accumulation whose error is far smaller at these
+sizes; the bound used is 3e-3.  Shapes span several 128 x 256 tiles, ragged
+edges in M, N and K, and batches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_07_gb300 as ns
+import oracle
+from nsutil import per_matrix_rel, random_bits, symmetric_bits, to_bits, to_dev, to_f64
+import ns_inputs
+
+pytestmark = pytest.mark.gpu
+KERNEL_TOL = 3e-3
+
+SHAPES = [(1, 8, 8), (3, 136, 264), (2, 256, 512), (2, 264, 136), (1, 392, 200), (1, 200, 392),
+          (2, 128, 128), (1, 520, 1040), (1, 1040, 520)]
+
+
+def f64(bits):
+    return ns_inputs.bf16_bits_to_f64(bits)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_normalize(shape):
+    bits = random_bits(shape, seed=sum(shape))
+    G = to_dev(bits)
+    ws = ns.alloc_workspace(*shape)
+    X = ns.muon_ns_normalize(G, ws, eps=1e-7)
+    off, nb = ns.workspace_region(*shape, ns._lib.WS_NORMS)
+    norms = ws[off:off + nb].view(torch.float32).cpu().numpy()
+    g = f64(bits)
+    for k in range(shape[0]):
+        nu = oracle.frobenius_norm(g[k])
+        assert abs(norms[k] - nu) <= 1e-5 * nu
+    ref = np.stack([oracle.normalize(g[k], 1e-7) for k in range(shape[0])])
+    assert max(per_matrix_rel(to_f64(X), ref)) <= KERNEL_TOL
+    # Elementwise: one bf16 rounding of the scaled value.
+    assert np.all(np.abs(to_f64(X) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+
+
+def gram_ref(x):
+    return oracle.gram(x) if x.shape[0] <= x.shape[1] else oracle.gram(x.T)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_gram(shape):
+    bits = random_bits(shape, seed=7 + sum(shape), scale=0.05)
+    A = ns.muon_ns_gram(to_dev(bits))
+    torch.cuda.synchronize()
+    a = to_bits(A)
+    np.testing.assert_array_equal(a, np.swapaxes(a, 1, 2))  # bit-symmetric
+    x = f64(bits)
+    ref = np.stack([gram_ref(x[k]) for k in range(shape[0])])
+    assert max(per_matrix_rel(f64(a), ref)) <= KERNEL_TOL
+
+
+@pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1040)])
+def test_poly(batch, m):
+    bits = symmetric_bits(batch, m, seed=m)
+    b, c = -4.7750, 2.0315
+    B = ns.muon_ns_poly(to_dev(bits), b, c)
+    torch.cuda.synchronize()
+    bb = to_bits(B)
+    np.testing.assert_array_equal(bb, np.swapaxes(bb, 1, 2))
+    a = f64(bits)
+    ref = np.stack([oracle.poly(a[k], b, c) for k in range(batch)])
+    assert max(per_matrix_rel(f64(bb), ref)) <= KERNEL_TOL
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_update(shape):
+    batch, r, c = shape
+    m = min(r, c)
+    xbits = random_bits(shape, seed=11 + r, scale=0.05)
+    bbits = symmetric_bits(batch, m, seed=13 + c, scale=0.05)
+    a = 3.4445
+    Xn = ns.muon_ns_update(to_dev(xbits), to_dev(bbits), a)
+    torch.cuda.synchronize()
+    x, B = f64(xbits), f64(bbits)
+    ref = []
+    for k in range(batch):
+        if r <= c:
+            ref.append(oracle.update(x[k], B[k], a))
+        else:  # tall input kept in its own orientation: (a X^T + B X^T)^T
+            ref.append(oracle.update(x[k].T, B[k], a).T)
+    assert max(per_matrix_rel(to_f64(Xn), np.stack(ref))) <= KERNEL_TOL
+
+
+def test_device_error_word_stays_clear():
+    shape = (2, 256, 512)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    X = to_dev(random_bits(shape, seed=3))
+    A = ns.muon_ns_gram(X, device_error=err)
+    B = ns.muon_ns_poly(A, -4.775, 2.0315, device_error=err)
+    ns.muon_ns_update(X, B, 3.4445, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0

@@ -1,0 +1,214 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+  * the library loads and exports every function include/muon_ns.h declares;
+  * argument validation returns the documented status codes before touching a
+    device;
+  * the tile scheduler (the kernels' own decode, through the ABI) covers every
+    output tile of a launch exactly once, and a model of the epilogue's store
+    predicates writes every output element exactly once, in bounds.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_07_gb300 as ns
+from newton_schulz_07_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "muon_ns.h")
+TILE_M, TILE_N = 128, 256
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_ns\w*)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    L = _lib.lib()
+    declared = header_functions()
+    assert len(declared) >= 15
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in muon_ns.h but not exported"
+    assert set(declared) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_version_and_status_strings():
+    L = _lib.lib()
+    assert L.muon_ns_version().decode() == ns.__version__
+    for code in range(7):
+        assert L.muon_ns_status_string(code)
+    assert L.muon_ns_status_string(99).decode() == "unknown status"
+
+
+def test_launch_count():
+    L = _lib.lib()
+    assert [L.muon_ns_launches_per_call(s) for s in (0, 1, 5)] == [2, 5, 17]
+    assert L.muon_ns_launches_per_call(-1) == -1
+
+
+def _ws(b, r, c):
+    n = ctypes.c_size_t(0)
+    s = _lib.lib().muon_ns_workspace_size(b, r, c, ctypes.byref(n))
+    return s, n.value
+
+
+def test_workspace_size_and_regions():
+    s, total = _ws(4, 256, 512)
+    assert s == _lib.OK
+    regions = {}
+    for reg in range(6):
+        regions[reg] = ns.workspace_region(4, 256, 512, reg)
+    assert regions[_lib.WS_TOTAL] == (0, total)
+    assert regions[_lib.WS_X][1] == 4 * 256 * 512 * 2
+    assert regions[_lib.WS_GRAM][1] == regions[_lib.WS_POLY][1] == 4 * 256 * 256 * 2
+    # Regions are disjoint, aligned and inside the workspace.
+    spans = sorted((o, o + n) for r, (o, n) in regions.items() if r != _lib.WS_TOTAL)
+    for (o0, e0), (o1, _) in zip(spans, spans[1:]):
+        assert e0 <= o1
+    for r in (_lib.WS_X, _lib.WS_GRAM, _lib.WS_POLY):
+        assert regions[r][0] % 1024 == 0
+        assert regions[r][0] + regions[r][1] <= total
+    # Tall input: the Gram is cols x cols.
+    assert ns.workspace_region(2, 512, 256, _lib.WS_GRAM)[1] == 2 * 256 * 256 * 2
+    assert _ws(0, 256, 512) == (_lib.OK, 0)
+
+
+@pytest.mark.parametrize("b,r,c,code", [
+    (-1, 8, 8, _lib.ERR_INVALID_ARG),
+    (1, -8, 8, _lib.ERR_INVALID_ARG),
+    (1, 12, 16, _lib.ERR_ALIGNMENT),
+    (1, 16, 20, _lib.ERR_ALIGNMENT),
+    (1, (1 << 20) + 8, 8, _lib.ERR_INVALID_ARG),
+    (1, 65536, 65536, _lib.ERR_INVALID_ARG),
+])
+def test_shape_validation(b, r, c, code):
+    assert _ws(b, r, c)[0] == code
+    L = _lib.lib()
+    p = ctypes.c_void_p(4096)
+    assert L.muon_ns_ws(p, p, b, r, c, 5, None, 1e-7, p, 1 << 40, None) == code
+    assert L.muon_ns(p, p, b, r, c, 5, None, 1e-7, None) == code
+
+
+def _call_ws(**kw):
+    L = _lib.lib()
+    args = dict(G=4096, out=4096, batch=2, rows=64, cols=128, steps=5, coeffs=None, eps=1e-7,
+                ws=4096, wsb=1 << 30, stream=None)
+    args.update(kw)
+    cf = None
+    if args["coeffs"] is not None:
+        cf = ctypes.cast((ctypes.c_float * 3)(*args["coeffs"]), ctypes.POINTER(ctypes.c_float))
+    return L.muon_ns_ws(ctypes.c_void_p(args["G"]), ctypes.c_void_p(args["out"]), args["batch"], args["rows"],
+                        args["cols"], args["steps"], cf, args["eps"], ctypes.c_void_p(args["ws"]),
+                        args["wsb"], args["stream"])
+
+
+def test_argument_validation_codes():
+    assert _call_ws(G=0) == _lib.ERR_INVALID_ARG
+    assert _call_ws(out=0) == _lib.ERR_INVALID_ARG
+    assert _call_ws(steps=-1) == _lib.ERR_INVALID_ARG
+    assert _call_ws(eps=-1.0) == _lib.ERR_INVALID_ARG
+    assert _call_ws(eps=float("nan")) == _lib.ERR_INVALID_ARG
+    assert _call_ws(eps=float("inf")) == _lib.ERR_INVALID_ARG
+    assert _call_ws(coeffs=(1.0, float("nan"), 1.0)) == _lib.ERR_INVALID_ARG
+    assert _call_ws(G=4098) == _lib.ERR_ALIGNMENT
+    assert _call_ws(out=4104) == _lib.ERR_ALIGNMENT
+    assert _call_ws(ws=0) == _lib.ERR_WORKSPACE
+    assert _call_ws(wsb=16) == _lib.ERR_WORKSPACE
+    assert _call_ws(ws=4096 + 16) == _lib.ERR_ALIGNMENT
+    # Empty problems succeed without touching pointers or the device.
+    assert _call_ws(G=0, out=0, ws=0, batch=0) == _lib.OK
+    assert _call_ws(G=0, out=0, ws=0, rows=0) == _lib.OK
+    L = _lib.lib()
+    assert L.muon_ns_gram(None, None, 1, 16, 12, None, None) == _lib.ERR_ALIGNMENT
+    assert L.muon_ns_gram(None, None, 1, 16, 16, None, None) == _lib.ERR_INVALID_ARG
+    p = ctypes.c_void_p(4096)
+    assert L.muon_ns_poly(p, p, 1, 16, 1.0, 1.0, None, None) == _lib.ERR_INVALID_ARG  # B == A
+    assert L.muon_ns_update(p, ctypes.c_void_p(8192), p, 1, 16, 16, 1.0, None, None) == _lib.ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_is_unsupported():
+    assert _call_ws() == _lib.ERR_UNSUPPORTED_DEVICE
+    assert _lib.lib().muon_ns_device_supported(-1) == _lib.ERR_UNSUPPORTED_DEVICE
+
+
+# ---------------------------------------------------------------- scheduler --
+
+def tiles(kind, batch, M, N):
+    L = _lib.lib()
+    total = L.muon_ns_tile_count(kind, batch, M, N)
+    b, i, j = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    out = []
+    for t in range(total):
+        assert L.muon_ns_tile_coords(kind, batch, M, N, t, ctypes.byref(b), ctypes.byref(i), ctypes.byref(j)) == 0
+        out.append((b.value, i.value, j.value))
+    return out
+
+
+SYM_SIZES = [8, 120, 128, 136, 248, 256, 264, 384, 392, 512, 640, 768, 1000, 1536, 2056]
+
+
+@pytest.mark.parametrize("m", SYM_SIZES)
+def test_triangle_schedule_covers_lower_triangle_once(m):
+    ts = tiles(0, 2, m, m)
+    tm = -(-m // TILE_M)
+    T = -(-m // TILE_N)
+    expect = {(b, I, J) for b in range(2) for I in range(tm) for J in range(T) if J <= I // 2}
+    assert len(ts) == len(set(ts)) == len(expect)
+    assert set(ts) == expect
+    # Matrix-major order.
+    assert [b for b, _, _ in ts] == sorted(b for b, _, _ in ts)
+
+
+def test_triangle_tile_counts():
+    L = _lib.lib()
+    assert L.muon_ns_tile_count(0, 128, 1536, 1536) == 128 * 42
+    assert L.muon_ns_tile_count(0, 1, 8192, 8192) == 32 * 33
+    assert L.muon_ns_tile_count(0, 1, 768, 768) == 12
+    assert L.muon_ns_tile_count(0, 1, 16, 8) == -1
+
+
+@pytest.mark.parametrize("M,N", [(8, 8), (128, 256), (136, 264), (1536, 2048), (2048, 768), (400, 1000),
+                                 (1100, 520)])
+def test_grid_schedule_covers_every_tile_once(M, N):
+    ts = tiles(1, 3, M, N)
+    tm, tn = -(-M // TILE_M), -(-N // TILE_N)
+    expect = {(b, I, J) for b in range(3) for I in range(tm) for J in range(tn)}
+    assert len(ts) == len(set(ts)) and set(ts) == expect
+
+
+def _epilogue_writes(kind, M, N, ts):
+    """Model of the epilogue store predicates: counts how often each output
+    element is written (direct and mirrored stores) over all tiles."""
+    count = np.zeros((M, N), dtype=np.int32)
+    r = np.arange(TILE_M)[:, None]
+    c = np.arange(TILE_N)[None, :]
+    for _, I, J in ts:
+        gi = I * TILE_M + r
+        gj = J * TILE_N + c
+        inb = (gi < M) & (gj < N)
+        if kind == 1:
+            np.add.at(count, (np.broadcast_to(gi, inb.shape)[inb], np.broadcast_to(gj, inb.shape)[inb]), 1)
+            continue
+        d = inb & (gj <= gi)
+        np.add.at(count, (np.broadcast_to(gi, d.shape)[d], np.broadcast_to(gj, d.shape)[d]), 1)
+        mi = inb & (gj < gi)
+        np.add.at(count, (np.broadcast_to(gj, mi.shape)[mi], np.broadcast_to(gi, mi.shape)[mi]), 1)
+    return count
+
+
+@pytest.mark.parametrize("m", [8, 136, 256, 392, 640, 1000])
+def test_symmetric_epilogue_writes_each_element_once(m):
+    ts = [t for t in tiles(0, 1, m, m)]
+    assert np.all(_epilogue_writes(0, m, m, ts) == 1)
+
+
+@pytest.mark.parametrize("M,N", [(8, 8), (136, 264), (400, 1000)])
+def test_full_epilogue_writes_each_element_once(M, N):
+    assert np.all(_epilogue_writes(1, M, N, tiles(1, 1, M, N)) == 1)
