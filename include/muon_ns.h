@@ -176,6 +176,26 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, fl
 int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int batch, int rows,
                    int cols, float a, int* device_error, cudaStream_t stream);
 
+/* X = bf16(G * (1 / (||G_k||_F + eps))) exactly as muon_ns_normalize(), for
+ * callers that cannot allocate device memory (plugins handed only their
+ * buffers, hosts whose allocator forbids cudaMalloc, loops that cannot take
+ * cudaMalloc's synchronisation).  It allocates nothing and takes no
+ * workspace: its scratch is a 1 MiB static device array of the library, held
+ * by every GPU that loads it until the process exits.  The pages have no
+ * counterpart; this is a deployment variant of the first NS step.
+ *   - Size limit: 4 * batch * (ceil(rows * cols / 16384) + 2) bytes, each of
+ *     the three parts rounded up to 256, must fit in 1 MiB; larger problems
+ *     return MUON_NS_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one array; it keeps the last call's contents and
+ *     the call zeroes what must start at zero.  Calls that overlap on the GPU
+ *     (different streams, no ordering) race on it and give wrong results.
+ *   - Other arguments, errors and aliasing as for muon_ns_normalize(). */
+int muon_ns_normalize_static(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols,
+                             float eps, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Host-only helpers (no GPU needed).
  * ------------------------------------------------------------------------- */

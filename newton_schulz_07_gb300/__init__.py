@@ -12,6 +12,7 @@ from .ns import (  # noqa: F401
     muon_ns,
     muon_ns_gram,
     muon_ns_normalize,
+    muon_ns_normalize_static,
     muon_ns_poly,
     muon_ns_update,
     read_error,

@@ -543,3 +543,72 @@ int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Normalisation without any allocation.
+//
+// Some callers cannot allocate device memory: a plugin that a host program
+// hands only its input and output buffers, a framework whose caching
+// allocator owns all device memory and forbids direct cudaMalloc, or a
+// latency-bound loop that cannot afford cudaMalloc's implicit device
+// synchronisation.  muon_ns_normalize_static() serves them: the norm kernel's
+// scratch (per-matrix tickets, per-chunk partial sums and the norms) lives in
+// the fixed array below, which every GPU that loads this library holds until
+// the process exits.
+// ---------------------------------------------------------------------------
+
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+std::mutex g_static_mu;
+void* g_static_addr[64];
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_ns_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+// Device address of the static scratch on the current device `dev`, looked up
+// once per device (the array's name is only a host-side stand-in in host code).
+int static_scratch_address(int dev, uint8_t** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_ns_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MUON_NS_ERR_CUDA;
+    }
+    g_static_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_static_addr[dev]);
+  return MUON_NS_OK;
+}
+
+}  // namespace
+
+extern "C" int muon_ns_normalize_static(const muon_bf16* G, muon_bf16* X, int batch, int rows,
+                                        int cols, float eps, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MUON_NS_ERR_INVALID_ARG;
+  if (empty) return MUON_NS_OK;
+  if (!G || !X) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(X)) return MUON_NS_ERR_ALIGNMENT;
+  // Scratch layout inside the static array: tickets, partial sums, norms.
+  Layout L = make_layout(p);
+  L.error = 0;
+  L.tickets = 0;
+  L.partials = round_up(4 * static_cast<size_t>(p.batch), 256);
+  L.norms = round_up(L.partials + 4 * static_cast<size_t>(p.batch) * L.chunks, 256);
+  if (L.norms + 4 * static_cast<size_t>(p.batch) > kStaticScratchBytes) return MUON_NS_ERR_WORKSPACE;
+  DevInfo d;
+  int dev = 0;
+  if ((s = current_device_info(&d, &dev)) != MUON_NS_OK) return s;
+  uint8_t* scratch = nullptr;
+  if ((s = static_scratch_address(dev, &scratch)) != MUON_NS_OK) return s;
+  // The tickets are zeroed by run_normalize on `stream`; partials and norms
+  // are overwritten.
+  return run_normalize(p, L, G, X, eps, scratch, stream);
+}

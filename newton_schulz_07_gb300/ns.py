@@ -149,3 +149,16 @@ def read_error(workspace: torch.Tensor, clear: bool = False) -> int:
 
 def launches_per_call(steps: int) -> int:
     return _lib.lib().muon_ns_launches_per_call(steps)
+
+
+def muon_ns_normalize_static(G: torch.Tensor, eps: float = DEFAULT_EPS, X: torch.Tensor | None = None) -> torch.Tensor:
+    """muon_ns_normalize without a workspace: for callers that cannot allocate
+    device memory; its scratch is the library's 1 MiB static device array
+    (see include/muon_ns.h for the size limit and the sharing rules)."""
+    _check_bf16(G, "G")
+    b, r, c = _shape3(G)
+    X = torch.empty_like(G) if X is None else X
+    with torch.cuda.device(G.device):
+        _lib.check(_lib.lib().muon_ns_normalize_static(_ptr(G), _ptr(X), b, r, c, float(eps), _stream(G.device)),
+                   "muon_ns_normalize_static")
+    return X
