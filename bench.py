@@ -317,6 +317,7 @@ def main():
     b_buf = torch.empty_like(a_buf)
     x_bufs = [torch.empty_like(G), torch.empty_like(G)]
     err_word = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_buf = torch.empty((w.batch, w.m), dtype=torch.float32, device=dev)
     a, b, c = ns.DEFAULT_COEFFS
     for it in range(nb + 2):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
@@ -327,9 +328,9 @@ def main():
         for s in range(5):
             ns.muon_ns_gram(x_bufs[cur], A=a_buf, device_error=err_word)
             ev[2 + 3 * s].record(stream)
-            ns.muon_ns_poly(a_buf, b, c, B=b_buf, device_error=err_word)
+            ns.muon_ns_poly(a_buf, b, c, B=b_buf, diag=d_buf, device_error=err_word)
             ev[3 + 3 * s].record(stream)
-            ns.muon_ns_update(x_bufs[cur], b_buf, a, Xn=x_bufs[1 - cur], device_error=err_word)
+            ns.muon_ns_update(x_bufs[cur], b_buf, a, Xn=x_bufs[1 - cur], diag=d_buf, device_error=err_word)
             ev[4 + 3 * s].record(stream)
             cur = 1 - cur
         torch.cuda.synchronize()
@@ -395,7 +396,7 @@ def main():
     per_shape = None
     if not args.no_per_shape and world == 1:
         per_shape = {}
-        del a_buf, b_buf, x_bufs
+        del a_buf, b_buf, x_bufs, d_buf
         for name, ow in ns_inputs.WORKLOADS.items():
             if name == w.name:
                 continue

@@ -26,7 +26,10 @@
  * epilogue of prime-rl PR #3873 (Results, note under the microbenchmark).
  * A and B are stored bit-symmetric: one triangle is computed and mirrored
  * (prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381 "Add
- * --muon-use-syrk option", Summary).
+ * --muon-use-syrk option", Summary).  The diagonal of B is kept in fp32
+ * (B = D + O, O bf16 with a zero diagonal) and the update applies (a + D)
+ * in its fp32 epilogue: the same arithmetic, with the part of B that
+ * dominates near convergence kept out of bf16 rounding.
  *
  * Conventions for every entry point below:
  *   - Matrices are contiguous row-major stacks [batch][rows][cols] of raw
@@ -98,7 +101,8 @@ enum {
   MUON_NS_WS_NORMS = 2,   /* fp32 [batch]: ||G_k||_F of the last call */
   MUON_NS_WS_X = 3,       /* bf16 [batch][rows][cols]: ping-pong iterate */
   MUON_NS_WS_GRAM = 4,    /* bf16 [batch][m][m]: A of the last step, m = min(rows, cols) */
-  MUON_NS_WS_POLY = 5     /* bf16 [batch][m][m]: B of the last step */
+  MUON_NS_WS_POLY = 5,    /* bf16 [batch][m][m]: off-diagonal part of B of the last step */
+  MUON_NS_WS_DIAG = 6     /* fp32 [batch][m]: diagonal of B of the last step */
 };
 
 /* Size of the workspace muon_ns_ws() needs for this problem, in bytes.
@@ -164,17 +168,26 @@ int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols
 
 /* B = b A + c (A A) for a bit-symmetric A, bf16 [batch][m][m].  A A is formed
  * as A A^T (equal for a bit-symmetric A) over lower-triangle tiles; the
- * epilogue reads A and computes in fp32; B is bit-symmetric.  B != A. */
-int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, float c,
-                 int* device_error, cudaStream_t stream);
+ * epilogue reads A and computes in fp32; B is bit-symmetric.  B != A.
+ *   diag  NULL: B is stored whole in bf16.
+ *         Non-NULL (device fp32 [batch][m], 16-byte aligned): B's diagonal is
+ *         written here in fp32 and zeros are stored on B's bf16 diagonal, i.e.
+ *         B = diag(D) + O with O bf16 and zero-diagonal.  muon_ns_ws does this:
+ *         near convergence B is close to a multiple of the identity and its
+ *         diagonal is the part bf16 would round worst. */
+int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
+                 float c, int* device_error, cudaStream_t stream);
 
 /* The update of the iterate, in the input orientation, with m = min(rows, cols):
  *   rows <= cols:  Xn = a X + B X     (B is rows x rows)
  *   rows >  cols:  Xn = a X + X B     (B is cols x cols; this is (a X^T + B X^T)^T
  *                                      for the bit-symmetric B)
- * fp32 epilogue reading X.  Xn must not overlap X or B. */
-int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int batch, int rows,
-                   int cols, float a, int* device_error, cudaStream_t stream);
+ * fp32 epilogue reading X.  Xn must not overlap X or B.
+ *   diag  NULL, or the fp32 diagonal written by muon_ns_poly (then B's stored
+ *         diagonal must be zero): the epilogue applies (a + diag_i) to X in
+ *         fp32, row i for rows <= cols, column i for rows > cols. */
+int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
+                   int batch, int rows, int cols, float a, int* device_error, cudaStream_t stream);
 
 /* X = bf16(G * (1 / (||G_k||_F + eps))) exactly as muon_ns_normalize(), for
  * callers that cannot allocate device memory (plugins handed only their

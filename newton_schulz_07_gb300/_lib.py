@@ -19,7 +19,7 @@ ERR_WORKSPACE = 4
 ERR_CUDA = 5
 ERR_TIMEOUT = 6
 
-WS_TOTAL, WS_ERROR, WS_NORMS, WS_X, WS_GRAM, WS_POLY = range(6)
+WS_TOTAL, WS_ERROR, WS_NORMS, WS_X, WS_GRAM, WS_POLY, WS_DIAG = range(7)
 
 _c_int, _c_ll, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
 _pf = ctypes.POINTER(ctypes.c_float)
@@ -40,8 +40,8 @@ SIGNATURES = {
     "muon_ns_normalize": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_normalize_static": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp]),
     "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
-    "muon_ns_poly": (_c_int, [_vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
-    "muon_ns_update": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _vp]),
+    "muon_ns_poly": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
+    "muon_ns_update": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _vp]),
     "muon_ns_launches_per_call": (_c_int, [_c_int]),
     "muon_ns_tile_count": (_c_ll, [_c_int, _c_int, _c_int, _c_int]),
     "muon_ns_tile_coords": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_ll, _pi, _pi, _pi]),

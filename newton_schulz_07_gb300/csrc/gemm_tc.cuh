@@ -6,6 +6,12 @@
 // accumulation in TMEM by tcgen05.mma (M = 128, N = 256, K = 16 per
 // instruction), fp32 epilogue, one rounding to bf16.
 //
+// With the optional fp32 diagonal (GemmArgs::diag_out / diag_in) the
+// polynomial product stores B = D + O as an fp32 vector D = diag(B) and a bf16
+// matrix O with zero diagonal, and the update computes (a + D) X + O X; near
+// convergence B is close to a multiple of the identity, so this keeps the
+// dominant part of B out of bf16 rounding.
+//
 // Template parameters:
 //   A_MN  the A operand is stored MN-major ([k][i], i contiguous) instead of
 //         K-major ([i][k], k contiguous);
@@ -68,6 +74,14 @@ struct GemmArgs {
   long long ld;
   long long bstride;
   float alpha, beta;
+  // Diagonal kept in fp32 (both optional):
+  //   diag_out  SYM only: the fp32 value of each diagonal element is written to
+  //             diag_out[b * M + i] and 0 is stored on the bf16 diagonal;
+  //   diag_in   the addend coefficient becomes beta + diag_in[...], indexed by
+  //             the output row (diag_per_col == 0) or column (== 1).
+  float* diag_out;
+  const float* diag_in;
+  int diag_per_col;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -300,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           args.addend ? args.addend + static_cast<long long>(b) * args.bstride : nullptr;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * kTileN);
+      // Addend coefficient for the whole row (row-indexed diagonal or none).
+      float row_coef = args.beta;
+      if (!SYM && args.diag_in != nullptr && !args.diag_per_col && row_ok)
+        row_coef += __ldg(args.diag_in + static_cast<long long>(b) * args.M + gi);
 
 #pragma unroll 1
       for (int c = 0; c < kTileN / 32; ++c) {
@@ -314,6 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
         if (addm != nullptr) {
+          float cf[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cf[j] = row_coef;
+          if (!SYM && args.diag_in != nullptr && args.diag_per_col) {
+            const float4* dp = reinterpret_cast<const float4*>(
+                args.diag_in + static_cast<long long>(b) * args.N + gj0);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (gj0 + 4 * g + 4 <= args.N) {
+                const float4 d = __ldg(dp + g);
+                cf[4 * g + 0] = args.beta + d.x;
+                cf[4 * g + 1] = args.beta + d.y;
+                cf[4 * g + 2] = args.beta + d.z;
+                cf[4 * g + 3] = args.beta + d.w;
+              }
+            }
+          }
           const uint4* src = reinterpret_cast<const uint4*>(addm + gi * args.ld + gj0);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -322,11 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
-                f[8 * g + 2 * h] = fmaf(args.beta, detail::bf16_lo(ws[h]), f[8 * g + 2 * h]);
-                f[8 * g + 2 * h + 1] = fmaf(args.beta, detail::bf16_hi(ws[h]), f[8 * g + 2 * h + 1]);
+                f[8 * g + 2 * h] = fmaf(cf[8 * g + 2 * h], detail::bf16_lo(ws[h]), f[8 * g + 2 * h]);
+                f[8 * g + 2 * h + 1] =
+                    fmaf(cf[8 * g + 2 * h + 1], detail::bf16_hi(ws[h]), f[8 * g + 2 * h + 1]);
               }
             }
           }
+        }
+        if (SYM && args.diag_out != nullptr && gi >= gj0 && gi < gj0 + 32) {
+          // The diagonal element goes to the fp32 side vector; 0 is stored.
+          float dval = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (gj0 + j == gi) {
+              dval = f[j];
+              f[j] = 0.0f;
+            }
+          }
+          args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
         }
         uint32_t hv[16];
 #pragma unroll

@@ -38,7 +38,7 @@ struct Problem {
 };
 
 struct Layout {
-  size_t error, tickets, partials, norms, x, a, b, total;
+  size_t error, tickets, partials, norms, diag, x, a, b, total;
   size_t x_bytes, a_bytes;
   int chunks;
 };
@@ -73,7 +73,9 @@ Layout make_layout(const Problem& p) {
   L.partials = off;
   off = round_up(off + 4 * static_cast<size_t>(p.batch) * L.chunks, 256);
   L.norms = off;
-  off = round_up(off + 4 * static_cast<size_t>(p.batch), 1024);
+  off = round_up(off + 4 * static_cast<size_t>(p.batch), 256);
+  L.diag = off;
+  off = round_up(off + 4 * static_cast<size_t>(p.batch) * p.m, 1024);
   L.x = off;
   L.x_bytes = 2 * static_cast<size_t>(p.batch) * p.R * p.C;
   off = round_up(off + L.x_bytes, 1024);
@@ -204,8 +206,8 @@ int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, int* err, int sms
   return to_status(mns::launch_sym_mnmn(ta, ta, a, grid_for(a, sms), st));
 }
 
-int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float b, float c,
-             int* err, int sms, cudaStream_t st) {
+int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float* diag, float b,
+             float c, int* err, int sms, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, m, m, batch, mns::kBlockK, mns::kTileM) ||
       !make_map(&tb, A, m, m, batch, mns::kBlockK, mns::kTileN))
@@ -215,11 +217,12 @@ int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float
   a.addend = A;
   a.alpha = c;
   a.beta = b;
+  a.diag_out = diag;
   return to_status(mns::launch_sym_kk(ta, tb, a, grid_for(a, sms), st));
 }
 
-int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, uint16_t* Xn, float alpha_x,
-               int* err, int sms, cudaStream_t st) {
+int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const float* diag,
+               uint16_t* Xn, float alpha_x, int* err, int sms, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!p.T) {
     // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
@@ -230,6 +233,8 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, uint16_t*
     a.out = Xn;
     a.addend = X;
     a.beta = alpha_x;
+    a.diag_in = diag;  // (a + D_i) scales row i of X
+    a.diag_per_col = 0;
     return to_status(mns::launch_full_kmn(ta, tb, a, grid_for(a, sms), st));
   }
   // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
@@ -240,6 +245,8 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, uint16_t*
   a.out = Xn;
   a.addend = X;
   a.beta = alpha_x;
+  a.diag_in = diag;  // Y D: (a + D_j) scales column j of Y
+  a.diag_per_col = 1;
   return to_status(mns::launch_full_kk(ta, tb, a, grid_for(a, sms), st));
 }
 
@@ -267,14 +274,15 @@ int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, 
   uint16_t* wsx = reinterpret_cast<uint16_t*>(ws + L.x);
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
   uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
+  float* D = reinterpret_cast<float*>(ws + L.diag);
   uint16_t* cur = (steps % 2 == 1) ? wsx : out;
   int s = run_normalize(p, L, G, cur, eps, ws, st);
   if (s != MUON_NS_OK) return s;
   for (int k = 0; k < steps; ++k) {
     uint16_t* nxt = (cur == out) ? wsx : out;
     if ((s = run_gram(p, cur, A, err, sms, st)) != MUON_NS_OK) return s;
-    if ((s = run_poly(p.batch, p.m, A, B, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-    if ((s = run_update(p, cur, B, nxt, abc[0], err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_poly(p.batch, p.m, A, B, D, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_update(p, cur, B, D, nxt, abc[0], err, sms, st)) != MUON_NS_OK) return s;
     cur = nxt;
   }
   return MUON_NS_OK;
@@ -358,6 +366,7 @@ int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* 
     case MUON_NS_WS_X: *offset = L.x; *bytes = L.x_bytes; break;
     case MUON_NS_WS_GRAM: *offset = L.a; *bytes = L.a_bytes; break;
     case MUON_NS_WS_POLY: *offset = L.b; *bytes = L.a_bytes; break;
+    case MUON_NS_WS_DIAG: *offset = L.diag; *bytes = 4 * static_cast<size_t>(p.batch) * p.m; break;
     default: return MUON_NS_ERR_INVALID_ARG;
   }
   return MUON_NS_OK;
@@ -494,8 +503,8 @@ int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols
   return run_gram(p, X, A, device_error, d.sms, stream);
 }
 
-int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, float c,
-                 int* device_error, cudaStream_t stream) {
+int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
+                 float c, int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, m, m, &p, &empty);
@@ -503,14 +512,14 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, int batch, int m, float b, fl
   if (!std::isfinite(b) || !std::isfinite(c)) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!A || !B || A == B) return MUON_NS_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B)) return MUON_NS_ERR_ALIGNMENT;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(diag)) return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_poly(p.batch, p.m, A, B, b, c, device_error, d.sms, stream);
+  return run_poly(p.batch, p.m, A, B, diag, b, c, device_error, d.sms, stream);
 }
 
-int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int batch, int rows,
-                   int cols, float a, int* device_error, cudaStream_t stream) {
+int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
+                   int batch, int rows, int cols, float a, int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, rows, cols, &p, &empty);
@@ -518,10 +527,11 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, muon_bf16* Xn, int ba
   if (!std::isfinite(a)) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!X || !B || !Xn || Xn == X || Xn == B) return MUON_NS_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(B) || !aligned16(Xn)) return MUON_NS_ERR_ALIGNMENT;
+  if (!aligned16(X) || !aligned16(B) || !aligned16(Xn) || !aligned16(diag))
+    return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_update(p, X, B, Xn, a, device_error, d.sms, stream);
+  return run_update(p, X, B, diag, Xn, a, device_error, d.sms, stream);
 }
 
 int muon_ns_launches_per_call(int steps) { return steps < 0 ? -1 : 2 + 3 * steps; }

@@ -114,27 +114,36 @@ def muon_ns_gram(X: torch.Tensor, A: torch.Tensor | None = None, device_error: t
 
 
 def muon_ns_poly(A: torch.Tensor, b: float, c: float, B: torch.Tensor | None = None,
-                 device_error: torch.Tensor | None = None):
+                 diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+    """B = b A + c A A.  With `diag` (fp32, batch*m elements) B's diagonal goes
+    there in fp32 and B's stored diagonal is zero."""
     _check_bf16(A, "A")
     bt, m, m2 = _shape3(A)
     if m != m2:
         raise ValueError("A must be square")
+    if diag is not None and (diag.dtype != torch.float32 or diag.numel() != bt * m or not diag.is_contiguous()):
+        raise ValueError("diag must be a contiguous float32 tensor of batch * m elements")
     B = torch.empty_like(A) if B is None else B
     with torch.cuda.device(A.device):
-        _lib.check(_lib.lib().muon_ns_poly(_ptr(A), _ptr(B), bt, m, float(b), float(c), _ptr(device_error),
-                                           _stream(A.device)), "muon_ns_poly")
+        _lib.check(_lib.lib().muon_ns_poly(_ptr(A), _ptr(B), _ptr(diag), bt, m, float(b), float(c),
+                                           _ptr(device_error), _stream(A.device)), "muon_ns_poly")
     return B
 
 
 def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor | None = None,
-                   device_error: torch.Tensor | None = None):
+                   diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+    """X' = a X + B X (X' = a X + X B for tall X).  With `diag` from
+    muon_ns_poly, B = diag(D) + B_stored."""
     _check_bf16(X, "X")
     _check_bf16(B, "B")
     bt, r, c = _shape3(X)
+    if diag is not None and (diag.dtype != torch.float32 or diag.numel() != bt * min(r, c)
+                             or not diag.is_contiguous()):
+        raise ValueError("diag must be a contiguous float32 tensor of batch * min(rows, cols) elements")
     Xn = torch.empty_like(X) if Xn is None else Xn
     with torch.cuda.device(X.device):
-        _lib.check(_lib.lib().muon_ns_update(_ptr(X), _ptr(B), _ptr(Xn), bt, r, c, float(a), _ptr(device_error),
-                                             _stream(X.device)), "muon_ns_update")
+        _lib.check(_lib.lib().muon_ns_update(_ptr(X), _ptr(B), _ptr(diag), _ptr(Xn), bt, r, c, float(a),
+                                             _ptr(device_error), _stream(X.device)), "muon_ns_update")
     return Xn
 
 

@@ -62,28 +62,48 @@ def test_gram(shape):
 
 
 @pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1040)])
-def test_poly(batch, m):
+@pytest.mark.parametrize("split_diag", [False, True])
+def test_poly(batch, m, split_diag):
     bits = symmetric_bits(batch, m, seed=m)
     b, c = -4.7750, 2.0315
-    B = ns.muon_ns_poly(to_dev(bits), b, c)
+    D = torch.full((batch, m), float("nan"), dtype=torch.float32, device="cuda") if split_diag else None
+    B = ns.muon_ns_poly(to_dev(bits), b, c, diag=D)
     torch.cuda.synchronize()
     bb = to_bits(B)
     np.testing.assert_array_equal(bb, np.swapaxes(bb, 1, 2))
     a = f64(bits)
     ref = np.stack([oracle.poly(a[k], b, c) for k in range(batch)])
-    assert max(per_matrix_rel(f64(bb), ref)) <= KERNEL_TOL
+    got = f64(bb)
+    if split_diag:
+        idx = np.arange(m)
+        assert np.all(bb[:, idx, idx] == 0)
+        d = D.cpu().numpy().astype(np.float64)
+        ref_d = ref[:, idx, idx]
+        # fp32 epilogue, no bf16 rounding: fp32 accumulation error only.
+        assert np.all(np.abs(d - ref_d) <= 1e-5 * np.abs(ref).max(axis=(1, 2))[:, None])
+        got[:, idx, idx] = d
+    assert max(per_matrix_rel(got, ref)) <= KERNEL_TOL
 
 
 @pytest.mark.parametrize("shape", SHAPES)
-def test_update(shape):
+@pytest.mark.parametrize("split_diag", [False, True])
+def test_update(shape, split_diag):
     batch, r, c = shape
     m = min(r, c)
     xbits = random_bits(shape, seed=11 + r, scale=0.05)
     bbits = symmetric_bits(batch, m, seed=13 + c, scale=0.05)
     a = 3.4445
-    Xn = ns.muon_ns_update(to_dev(xbits), to_dev(bbits), a)
-    torch.cuda.synchronize()
+    D = None
     x, B = f64(xbits), f64(bbits)
+    if split_diag:
+        idx = np.arange(m)
+        dvals = np.random.default_rng(r + c).uniform(-3.0, 1.0, size=(batch, m)).astype(np.float32)
+        bbits[:, idx, idx] = 0
+        B = f64(bbits)
+        B[:, idx, idx] = dvals
+        D = torch.from_numpy(dvals).cuda()
+    Xn = ns.muon_ns_update(to_dev(xbits), to_dev(bbits), a, diag=D)
+    torch.cuda.synchronize()
     ref = []
     for k in range(batch):
         if r <= c:
@@ -98,7 +118,8 @@ def test_device_error_word_stays_clear():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     X = to_dev(random_bits(shape, seed=3))
     A = ns.muon_ns_gram(X, device_error=err)
-    B = ns.muon_ns_poly(A, -4.775, 2.0315, device_error=err)
-    ns.muon_ns_update(X, B, 3.4445, device_error=err)
+    D = torch.empty((2, 256), dtype=torch.float32, device="cuda")
+    B = ns.muon_ns_poly(A, -4.775, 2.0315, diag=D, device_error=err)
+    ns.muon_ns_update(X, B, 3.4445, diag=D, device_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0

@@ -62,11 +62,12 @@ def test_workspace_size_and_regions():
     s, total = _ws(4, 256, 512)
     assert s == _lib.OK
     regions = {}
-    for reg in range(6):
+    for reg in range(7):
         regions[reg] = ns.workspace_region(4, 256, 512, reg)
     assert regions[_lib.WS_TOTAL] == (0, total)
     assert regions[_lib.WS_X][1] == 4 * 256 * 512 * 2
     assert regions[_lib.WS_GRAM][1] == regions[_lib.WS_POLY][1] == 4 * 256 * 256 * 2
+    assert regions[_lib.WS_DIAG][1] == 4 * 256 * 4
     # Regions are disjoint, aligned and inside the workspace.
     spans = sorted((o, o + n) for r, (o, n) in regions.items() if r != _lib.WS_TOTAL)
     for (o0, e0), (o1, _) in zip(spans, spans[1:]):
@@ -128,8 +129,10 @@ def test_argument_validation_codes():
     assert L.muon_ns_gram(None, None, 1, 16, 12, None, None) == _lib.ERR_ALIGNMENT
     assert L.muon_ns_gram(None, None, 1, 16, 16, None, None) == _lib.ERR_INVALID_ARG
     p = ctypes.c_void_p(4096)
-    assert L.muon_ns_poly(p, p, 1, 16, 1.0, 1.0, None, None) == _lib.ERR_INVALID_ARG  # B == A
-    assert L.muon_ns_update(p, ctypes.c_void_p(8192), p, 1, 16, 16, 1.0, None, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_poly(p, p, None, 1, 16, 1.0, 1.0, None, None) == _lib.ERR_INVALID_ARG  # B == A
+    assert L.muon_ns_poly(p, ctypes.c_void_p(8192), ctypes.c_void_p(12), 1, 16, 1.0, 1.0, None,
+                          None) == _lib.ERR_ALIGNMENT  # diag not 16-byte aligned
+    assert L.muon_ns_update(p, ctypes.c_void_p(8192), None, p, 1, 16, 16, 1.0, None, None) == _lib.ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
