@@ -23,7 +23,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const Gem
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  ns_tc_gemm<A_MN, B_MN, SYM><<<grid, kThreads, kSmemBytes, stream>>>(a, b, args);
+  ns_tc_gemm<A_MN, B_MN, SYM><<<grid, Epi<SYM>::kCtaThreads, kSmemBytes, stream>>>(a, b, args);
   return cudaGetLastError();
 }
 

@@ -28,12 +28,14 @@
 //   a X + B X        <false, true,  false>  X read MN-major
 //   a Y + Y B        <false, false, false>  B = B^T bitwise
 //
-// Roles (192 threads, one CTA per SM, persistent over the tile space):
+// Roles (64 + 32 * kEpiWarps threads, one CTA per SM, persistent):
 //   warp 0 lane 0   TMA producer: fills a kStages-deep ring of operand stages
 //   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma per stage into one of two
 //                   256-column TMEM accumulators, commits release the stage
-//   warps 2..5      epilogue: tcgen05.ld of their 32-lane quarter, fp32
-//                   epilogue, bf16 stores; then free the accumulator
+//   warps 2..       epilogue: each warp reads its 32-lane TMEM quarter for its
+//                   share of the columns (two warps per quarter by default),
+//                   prefetches the addend one 32-column chunk ahead, runs the
+//                   fp32 epilogue, stores bf16, then frees the accumulator
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // main loop of tile t + 1.
 //
@@ -55,8 +57,22 @@ namespace mns {
 
 constexpr int kBlockK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+// Epilogue warps (4 or 8: one or two per TMEM lane quarter).  The symmetric
+// products have the heavier epilogue (mirrored stores) per FLOP and take 8;
+// the update takes 4 (measured on GB300).
+#ifndef MNS_EPI_WARPS_SYM
+#define MNS_EPI_WARPS_SYM 8
+#endif
+#ifndef MNS_EPI_WARPS_FULL
+#define MNS_EPI_WARPS_FULL 4
+#endif
+template <bool SYM>
+struct Epi {
+  static constexpr int kWarps = SYM ? MNS_EPI_WARPS_SYM : MNS_EPI_WARPS_FULL;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kCtaThreads = 64 + kThreads;  // + producer warp + MMA warp
+  static constexpr int kChunksPerWarp = (kTileN / 32) / (kWarps / 4);
+};
 constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
 constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -88,12 +104,15 @@ struct GemmArgs {
 
 namespace detail {
 
+// Shared-memory addresses of the kernel's mbarriers, laid out consecutively:
+// full[kStages], empty[kStages], tfull[2], tempty[2], mma_done.
 struct Sync {
-  uint32_t full[kStages];
-  uint32_t empty[kStages];
-  uint32_t tfull[2];
-  uint32_t tempty[2];
-  uint32_t mma_done;
+  uint32_t base;
+  __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (kStages + s); }
+  __device__ __forceinline__ uint32_t tfull(int i) const { return base + 8u * (2 * kStages + i); }
+  __device__ __forceinline__ uint32_t tempty(int i) const { return base + 8u * (2 * kStages + 2 + i); }
+  __device__ __forceinline__ uint32_t mma_done() const { return base + 8u * (2 * kStages + 4); }
 };
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag, int* err) {
@@ -138,13 +157,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }  // namespace detail
 
 template <bool A_MN, bool B_MN, bool SYM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Epi<SYM>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  constexpr int kEpiWarps = Epi<SYM>::kWarps;
+  constexpr int kEpiThreads = Epi<SYM>::kThreads;
+  constexpr int kChunksPerWarp = Epi<SYM>::kChunksPerWarp;
+  __shared__ __align__(16) float colc_sh[SYM ? 1 : kEpiWarps][kChunksPerWarp * 32];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,28 +175,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   detail::Sync sy;
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) {
-    sy.full[s] = ptx::smem_u32(&bars[s]);
-    sy.empty[s] = ptx::smem_u32(&bars[kStages + s]);
-  }
-  sy.tfull[0] = ptx::smem_u32(&bars[2 * kStages + 0]);
-  sy.tfull[1] = ptx::smem_u32(&bars[2 * kStages + 1]);
-  sy.tempty[0] = ptx::smem_u32(&bars[2 * kStages + 2]);
-  sy.tempty[1] = ptx::smem_u32(&bars[2 * kStages + 3]);
-  sy.mma_done = ptx::smem_u32(&bars[2 * kStages + 4]);
+  sy.base = ptx::smem_u32(&bars[0]);
 
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(sy.full[s], 1);
-      ptx::mbar_init(sy.empty[s], 1);
+      ptx::mbar_init(sy.full(s), 1);
+      ptx::mbar_init(sy.empty(s), 1);
     }
-    ptx::mbar_init(sy.tfull[0], 1);
-    ptx::mbar_init(sy.tfull[1], 1);
-    ptx::mbar_init(sy.tempty[0], kEpiThreads);
-    ptx::mbar_init(sy.tempty[1], kEpiThreads);
-    ptx::mbar_init(sy.mma_done, 1);
+    ptx::mbar_init(sy.tfull(0), 1);
+    ptx::mbar_init(sy.tfull(1), 1);
+    ptx::mbar_init(sy.tempty(0), kEpiThreads);
+    ptx::mbar_init(sy.tempty(1), kEpiThreads);
+    ptx::mbar_init(sy.mma_done(), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
@@ -205,30 +219,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = J * kTileN;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.empty[stage], phase ^ 1u, abort_flag, args.err,
+          if (!detail::wait_bounded(sy.empty(stage), phase ^ 1u, abort_flag, args.err,
                                     args.budget)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(sy.full[stage], kStageBytes);
+          ptx::mbar_arrive_expect_tx(sy.full(stage), kStageBytes);
           const uint32_t sa = smem_base + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
           const int k0 = kb * kBlockK;
           if (A_MN) {
 #pragma unroll
             for (int c = 0; c < kTileM / kMnChunk; ++c)
-              ptx::tma_load_3d(sa + c * kMnChunkBytes, &tmA, sy.full[stage], row0 + c * kMnChunk,
+              ptx::tma_load_3d(sa + c * kMnChunkBytes, &tmA, sy.full(stage), row0 + c * kMnChunk,
                                k0, b);
           } else {
-            ptx::tma_load_3d(sa, &tmA, sy.full[stage], k0, row0, b);
+            ptx::tma_load_3d(sa, &tmA, sy.full(stage), k0, row0, b);
           }
           if (B_MN) {
 #pragma unroll
             for (int c = 0; c < kTileN / kMnChunk; ++c)
-              ptx::tma_load_3d(sb + c * kMnChunkBytes, &tmB, sy.full[stage], col0 + c * kMnChunk,
+              ptx::tma_load_3d(sb + c * kMnChunkBytes, &tmB, sy.full(stage), col0 + c * kMnChunk,
                                k0, b);
           } else {
-            ptx::tma_load_3d(sb, &tmB, sy.full[stage], k0, col0, b);
+            ptx::tma_load_3d(sb, &tmB, sy.full(stage), k0, col0, b);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -242,24 +256,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Wait for every copy still in flight before the CTA can exit.
 #pragma unroll
       for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) detail::drain_wait(sy.full[s], (issued_phase >> s) & 1u, args.budget);
+        if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, args.budget);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
+      constexpr uint32_t idesc_full = ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
+      constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t tphase = 0;
       for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
-        if (!detail::wait_bounded(sy.tempty[buf], tphase ^ 1u, abort_flag, args.err, args.budget))
+        // In a symmetric product, a tile on an even row tile I = 2J lies on the
+        // diagonal 256-column block with its right half entirely above the
+        // diagonal: only its left 128 columns are computed (N = 128).
+        uint32_t idesc = idesc_full;
+        if (SYM) {
+          int b, I, J;
+          tile_decode(sp, t, &b, &I, &J);
+          if ((I & 1) == 0 && J == (I >> 1)) idesc = idesc_half;
+        }
+        if (!detail::wait_bounded(sy.tempty(buf), tphase ^ 1u, abort_flag, args.err, args.budget))
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.full[stage], phase, abort_flag, args.err, args.budget)) {
+          if (!detail::wait_bounded(sy.full(stage), phase, abort_flag, args.err, args.budget)) {
             ok = false;
             break;
           }
@@ -274,25 +298,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : ptx::sw128_desc(sb + kk * 32, 16, 1024);
             ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(sy.empty[stage]);
+          ptx::mma_commit(sy.empty(stage));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(sy.tfull[buf]);
+        ptx::mma_commit(sy.tfull(buf));
         buf ^= 1;
         if (buf == 0) tphase ^= 1u;
       }
       // Every MMA issued by this thread has finished once this arrives.
-      ptx::mma_commit(sy.mma_done);
-      detail::drain_wait(sy.mma_done, 0, args.budget);
+      ptx::mma_commit(sy.mma_done());
+      detail::drain_wait(sy.mma_done(), 0, args.budget);
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Warp e = warp - 2 reads TMEM lane quarter q = warp % 4 (the lanes a warp
+    // may access) and owns kChunksPerWarp 32-column chunks of the tile.
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int c_begin = (e >> 2) * kChunksPerWarp;
     const int r_in_tile = q * 32 + lane;
+    float* colc = colc_sh[SYM ? 0 : e];
     int buf = 0;
     uint32_t tphase = 0;
     for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
@@ -300,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_decode(sp, t, &b, &I, &J);
       int ready = 0;
       if (lane == 0)
-        ready = detail::wait_bounded(sy.tfull[buf], tphase, abort_flag, args.err, args.budget) ? 1 : 0;
+        ready = detail::wait_bounded(sy.tfull(buf), tphase, abort_flag, args.err, args.budget) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       __syncwarp();
@@ -314,104 +343,125 @@ __global__ void __launch_bounds__(kThreads, 1)
           args.addend ? args.addend + static_cast<long long>(b) * args.bstride : nullptr;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * kTileN);
-      // Addend coefficient for the whole row (row-indexed diagonal or none).
+      const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
+      // Addend coefficient: per row (row-indexed diagonal or none) ...
       float row_coef = args.beta;
       if (!SYM && args.diag_in != nullptr && !args.diag_per_col && row_ok)
         row_coef += __ldg(args.diag_in + static_cast<long long>(b) * args.M + gi);
+      // ... or per column, staged in shared memory for this warp's columns.
+      const bool col_mode = !SYM && args.diag_in != nullptr && args.diag_per_col;
+      if (col_mode) {
+#pragma unroll
+        for (int v = 0; v < kChunksPerWarp; ++v) {
+          const int col = col_base + v * 32 + lane;
+          colc[v * 32 + lane] =
+              args.beta + (col < args.N ? __ldg(args.diag_in + static_cast<long long>(b) * args.N + col) : 0.0f);
+        }
+        __syncwarp();
+      }
+      // Addend values of one chunk (16-byte groups of 8 bf16), prefetched one
+      // chunk ahead so their latency overlaps the previous chunk's work.
+      auto load_addend = [&](int cc, uint4 (&dst)[4]) {
+        const int gj0 = col_base + cc * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
+        if (addm == nullptr || !row_ok || gj0 >= args.N || (SYM && gj0 > gi)) return;
+        const uint4* src = reinterpret_cast<const uint4*>(addm + gi * args.ld + gj0);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (gj0 + 8 * g + 8 <= args.N) dst[g] = __ldg(src + g);
+      };
+      uint4 av[4];
+      load_addend(0, av);
 
 #pragma unroll 1
-      for (int c = 0; c < kTileN / 32; ++c) {
-        const int gj0 = J * kTileN + c * 32;
+      for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+        const int gj0 = col_base + cc * 32;
         if (gj0 >= args.N) break;                   // warp-uniform
         if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
+        uint4 an[4];
+        if (cc + 1 < kChunksPerWarp) load_addend(cc + 1, an);
         uint32_t v[32];
-        ptx::tmem_ld_32cols(t_lane + c * 32, v);
+        ptx::tmem_ld_32cols(t_lane + static_cast<uint32_t>((c_begin + cc) * 32), v);
         ptx::tmem_wait_ld();
-        if (!row_ok) continue;
-        float f[32];
+        if (row_ok) {
+          float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
-        if (addm != nullptr) {
-          float cf[32];
+          for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
+          if (addm != nullptr) {
+            const uint32_t ws[16] = {av[0].x, av[0].y, av[0].z, av[0].w, av[1].x, av[1].y,
+                                     av[1].z, av[1].w, av[2].x, av[2].y, av[2].z, av[2].w,
+                                     av[3].x, av[3].y, av[3].z, av[3].w};
+            if (col_mode) {
+              const float4* cp = reinterpret_cast<const float4*>(colc + cc * 32);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) cf[j] = row_coef;
-          if (!SYM && args.diag_in != nullptr && args.diag_per_col) {
-            const float4* dp = reinterpret_cast<const float4*>(
-                args.diag_in + static_cast<long long>(b) * args.N + gj0);
+              for (int h = 0; h < 8; ++h) {
+                const float4 k4 = cp[h];
+                f[4 * h + 0] = fmaf(k4.x, detail::bf16_lo(ws[2 * h]), f[4 * h + 0]);
+                f[4 * h + 1] = fmaf(k4.y, detail::bf16_hi(ws[2 * h]), f[4 * h + 1]);
+                f[4 * h + 2] = fmaf(k4.z, detail::bf16_lo(ws[2 * h + 1]), f[4 * h + 2]);
+                f[4 * h + 3] = fmaf(k4.w, detail::bf16_hi(ws[2 * h + 1]), f[4 * h + 3]);
+              }
+            } else {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              if (gj0 + 4 * g + 4 <= args.N) {
-                const float4 d = __ldg(dp + g);
-                cf[4 * g + 0] = args.beta + d.x;
-                cf[4 * g + 1] = args.beta + d.y;
-                cf[4 * g + 2] = args.beta + d.z;
-                cf[4 * g + 3] = args.beta + d.w;
+              for (int h = 0; h < 16; ++h) {
+                f[2 * h] = fmaf(row_coef, detail::bf16_lo(ws[h]), f[2 * h]);
+                f[2 * h + 1] = fmaf(row_coef, detail::bf16_hi(ws[h]), f[2 * h + 1]);
               }
             }
           }
-          const uint4* src = reinterpret_cast<const uint4*>(addm + gi * args.ld + gj0);
+          if (SYM && args.diag_out != nullptr && gi >= gj0 && gi < gj0 + 32) {
+            // The diagonal element goes to the fp32 side vector; 0 is stored.
+            float dval = 0.0f;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (gj0 + 8 * g + 8 <= args.N) {
-              const uint4 w = __ldg(src + g);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                f[8 * g + 2 * h] = fmaf(cf[8 * g + 2 * h], detail::bf16_lo(ws[h]), f[8 * g + 2 * h]);
-                f[8 * g + 2 * h + 1] =
-                    fmaf(cf[8 * g + 2 * h + 1], detail::bf16_hi(ws[h]), f[8 * g + 2 * h + 1]);
+            for (int j = 0; j < 32; ++j) {
+              if (gj0 + j == gi) {
+                dval = f[j];
+                f[j] = 0.0f;
               }
             }
+            args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
           }
-        }
-        if (SYM && args.diag_out != nullptr && gi >= gj0 && gi < gj0 + 32) {
-          // The diagonal element goes to the fp32 side vector; 0 is stored.
-          float dval = 0.0f;
+          uint32_t hv[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (gj0 + j == gi) {
-              dval = f[j];
-              f[j] = 0.0f;
-            }
-          }
-          args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
-        }
-        uint32_t hv[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
-        uint16_t* rowp = outm + gi * args.ld + gj0;
-        if (!SYM) {
-          uint4* dst = reinterpret_cast<uint4*>(rowp);
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (gj0 + 8 * g + 8 <= args.N)
-              dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
-        } else {
-          if (gj0 + 31 <= gi && gj0 + 32 <= args.N) {
+          for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
+          uint16_t* rowp = outm + gi * args.ld + gj0;
+          if (!SYM) {
             uint4* dst = reinterpret_cast<uint4*>(rowp);
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-              dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
-          } else {
+              if (gj0 + 8 * g + 8 <= args.N)
+                dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
+          } else if (gj0 <= gi) {
+            if (gj0 + 31 <= gi && gj0 + 32 <= args.N) {
+              uint4* dst = reinterpret_cast<uint4*>(rowp);
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const long long gj = gj0 + j;
+                if (gj <= gi && gj < args.N)
+                  rowp[j] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+              }
+            }
+            // Mirror: (gj, gi) for gj < gi.  Lanes hold consecutive gi, so each
+            // store instruction writes 64 contiguous bytes of row gj.
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const long long gj = gj0 + j;
-              if (gj <= gi && gj < args.N)
-                rowp[j] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+              if (gj < gi && gj < args.N)
+                outm[gj * args.ld + gi] =
+                    static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
             }
           }
-          // Mirror: (gj, gi) for gj < gi.  Lanes hold consecutive gi, so each
-          // store instruction writes 64 contiguous bytes of row gj.
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const long long gj = gj0 + j;
-            if (gj < gi && gj < args.N)
-              outm[gj * args.ld + gi] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-          }
         }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) av[g] = an[g];
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(sy.tempty[buf]);
+      ptx::mbar_arrive(sy.tempty(buf));
       buf ^= 1;
       if (buf == 0) tphase ^= 1u;
     }
