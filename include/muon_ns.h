@@ -35,8 +35,8 @@
  *   - Matrices are contiguous row-major stacks [batch][rows][cols] of raw
  *     bf16 bit patterns (muon_bf16) in DEVICE memory owned by the caller.
  *   - rows and cols must be multiples of 8 and every device pointer must be
- *     16-byte aligned (16-byte rows for TMA; the same rule as prime-rl PR
- *     #3873, Summary item 1, "dimension not divisible by 8").  This is an
+ *     16-byte aligned (16-byte rows for TMA; prime-rl PR #3873, Summary
+ *     item 1, has the same divisible-by-8 rule).  This is an
  *     error (MUON_NS_ERR_ALIGNMENT), never a silent fallback (Megatron-LM PR
  *     #6381, "Version compatibility": a hard failure instead of a fallback).
  *   - batch == 0, rows == 0 or cols == 0 is an empty problem: MUON_NS_OK,

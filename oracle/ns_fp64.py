@@ -20,7 +20,7 @@ inside Dion's dense zeropower_via_newtonschulz5.  The step count 5 is the
 `ns_steps` default of param-decomp PR #978 ("stacked-NS Muon", What).  The
 batch semantics (the leading axis of a 3-D stack is a batch of independent
 matrices) are prime-rl PR #3873, Summary item 2, and param-decomp PR #978,
-What ("same-shape leaves are batched into ONE NS").
+What (leaves of one shape are stacked into a single NS).
 
 The pages name this function but do not print its constants.  The readings
 taken here, which the rest of the pages support:
@@ -29,8 +29,8 @@ taken here, which the rest of the pages support:
   * normalisation divides by ||G||_F + eps with eps = 1e-7;
   * the transpose is taken iff rows > cols (square inputs are not transposed);
   * every step runs in fp64 with no intermediate rounding.  prime-rl PR #3873
-    measures bf16 NS against "an fp32 NS with the same coefficients"; fp64 is
-    the stricter reference.
+    (Results) measures bf16 NS against an fp32 NS that uses the same
+    coefficients; fp64 is the stricter reference.
 
 Each step is a module-level function so that a test can replace one of them
 with a planted mistake and check that the pins catch it.  The matrix products
