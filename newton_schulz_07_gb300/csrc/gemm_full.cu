@@ -6,12 +6,14 @@ namespace mns {
 
 cudaError_t launch_full_kmn(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                             int grid, cudaStream_t stream) {
-  return launch_tc_gemm<false, true, false>(a, b, args, grid, stream);
+  return args.K <= 1024 ? launch_tc_gemm<false, true, false, 8>(a, b, args, grid, stream)
+                        : launch_tc_gemm<false, true, false, 4>(a, b, args, grid, stream);
 }
 
 cudaError_t launch_full_kk(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                            int grid, cudaStream_t stream) {
-  return launch_tc_gemm<false, false, false>(a, b, args, grid, stream);
+  return args.K <= 1024 ? launch_tc_gemm<false, false, false, 8>(a, b, args, grid, stream)
+                        : launch_tc_gemm<false, false, false, 4>(a, b, args, grid, stream);
 }
 
 }  // namespace mns

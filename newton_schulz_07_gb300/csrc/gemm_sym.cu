@@ -6,12 +6,12 @@ namespace mns {
 
 cudaError_t launch_sym_kk(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                           int grid, cudaStream_t stream) {
-  return launch_tc_gemm<false, false, true>(a, b, args, grid, stream);
+  return launch_tc_gemm<false, false, true, 8>(a, b, args, grid, stream);
 }
 
 cudaError_t launch_sym_mnmn(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                             int grid, cudaStream_t stream) {
-  return launch_tc_gemm<true, true, true>(a, b, args, grid, stream);
+  return launch_tc_gemm<true, true, true, 8>(a, b, args, grid, stream);
 }
 
 }  // namespace mns

@@ -57,18 +57,14 @@ namespace mns {
 
 constexpr int kBlockK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
-// Epilogue warps (4 or 8: one or two per TMEM lane quarter).  The symmetric
-// products have the heavier epilogue (mirrored stores) per FLOP and take 8;
-// the update takes 4 (measured on GB300).
-#ifndef MNS_EPI_WARPS_SYM
-#define MNS_EPI_WARPS_SYM 8
-#endif
-#ifndef MNS_EPI_WARPS_FULL
-#define MNS_EPI_WARPS_FULL 4
-#endif
-template <bool SYM>
+// Epilogue warps: 4 or 8, i.e. one or two per TMEM lane quarter.  The
+// symmetric products (mirrored stores) always take 8; the update takes 8 when
+// its contraction is short (K <= 1024, little main-loop time per tile to hide
+// the epilogue behind) and 4 otherwise (measured on GB300).
+template <int EPI_WARPS>
 struct Epi {
-  static constexpr int kWarps = SYM ? MNS_EPI_WARPS_SYM : MNS_EPI_WARPS_FULL;
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
+  static constexpr int kWarps = EPI_WARPS;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kCtaThreads = 64 + kThreads;  // + producer warp + MMA warp
   static constexpr int kChunksPerWarp = (kTileN / 32) / (kWarps / 4);
@@ -156,17 +152,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM>
-__global__ void __launch_bounds__(Epi<SYM>::kCtaThreads, 1)
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
+__global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  constexpr int kEpiWarps = Epi<SYM>::kWarps;
-  constexpr int kEpiThreads = Epi<SYM>::kThreads;
-  constexpr int kChunksPerWarp = Epi<SYM>::kChunksPerWarp;
+  constexpr int kEpiWarps = Epi<EPI_WARPS>::kWarps;
+  constexpr int kEpiThreads = Epi<EPI_WARPS>::kThreads;
+  constexpr int kChunksPerWarp = Epi<EPI_WARPS>::kChunksPerWarp;
   __shared__ __align__(16) float colc_sh[SYM ? 1 : kEpiWarps][kChunksPerWarp * 32];
 
   const int warp = threadIdx.x >> 5;
@@ -201,6 +197,12 @@ __global__ void __launch_bounds__(Epi<SYM>::kCtaThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  // Every CTA is resident from the start (one per SM), so the next kernel may
+  // be scheduled now: its CTAs take SMs as ours exit and finish their prologue
+  // meanwhile.  Nothing produced by the previous kernel is touched before this
+  // grid's dependency has completed.
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   const TileSpace& sp = args.space;
   const int num_kb = args.num_kb;

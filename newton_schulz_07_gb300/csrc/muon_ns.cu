@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include "muon_ns.h"
+#include "gemm_launch.cuh"
 #include "gemm_tc.cuh"
 #include "internal.h"
 #include "norm.cuh"
@@ -256,15 +257,17 @@ int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t
   if (cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
-  mns::ns_norm_partial<<<grid, mns::kNormThreads, 0, st>>>(
-      reinterpret_cast<const uint4*>(G), vec, L.chunks, reinterpret_cast<float*>(ws + L.partials),
-      reinterpret_cast<unsigned int*>(ws + L.tickets), reinterpret_cast<float*>(ws + L.norms));
-  if (cudaGetLastError() != cudaSuccess) return MUON_NS_ERR_CUDA;
-  mns::ns_scale<<<grid, mns::kNormThreads, 0, st>>>(reinterpret_cast<const uint4*>(G),
-                                                    reinterpret_cast<uint4*>(X), vec,
-                                                    reinterpret_cast<const float*>(ws + L.norms),
-                                                    eps);
-  return cudaGetLastError() == cudaSuccess ? MUON_NS_OK : MUON_NS_ERR_CUDA;
+  if (mns::launch_pdl(mns::ns_norm_partial, grid, dim3(mns::kNormThreads), 0, st,
+                      reinterpret_cast<const uint4*>(G), vec, L.chunks,
+                      reinterpret_cast<float*>(ws + L.partials),
+                      reinterpret_cast<unsigned int*>(ws + L.tickets),
+                      reinterpret_cast<float*>(ws + L.norms)) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
+  if (mns::launch_pdl(mns::ns_scale, grid, dim3(mns::kNormThreads), 0, st,
+                      reinterpret_cast<const uint4*>(G), reinterpret_cast<uint4*>(X), vec,
+                      reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
+  return MUON_NS_OK;
 }
 
 int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, int steps,

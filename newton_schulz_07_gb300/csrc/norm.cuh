@@ -23,6 +23,8 @@
 
 #include <cuda_bf16.h>
 
+#include "ptx.cuh"
+
 namespace mns {
 
 constexpr int kNormThreads = 256;
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(kNormThreads)
                     float* __restrict__ norms) {
   __shared__ float red[kNormThreads / 32];
   __shared__ int is_last;
+  ptx::griddep_wait();
   const int b = blockIdx.y;
   const int chunk = blockIdx.x;
   const uint4* g = G + static_cast<long long>(b) * vec_per_matrix;
@@ -102,6 +105,8 @@ __global__ void __launch_bounds__(kNormThreads)
 __global__ void __launch_bounds__(kNormThreads)
     ns_scale(const uint4* G, uint4* X, long long vec_per_matrix, const float* __restrict__ norms,
              float eps) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int b = blockIdx.y;
   const float s = 1.0f / (norms[b] + eps);
   const uint4* g = G + static_cast<long long>(b) * vec_per_matrix;

@@ -65,6 +65,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ------------------------------------------------- programmatic launches --
+
+// Wait until the grid this one depends on (the previous kernel in the stream,
+// launched with programmatic stream serialisation) has completed and its
+// memory is visible.  A no-op for a normal launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the dependent grid to be scheduled now (its CTAs start their
+// prologue and then block in griddep_wait until this grid completes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05 --
 
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
