@@ -29,8 +29,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
-cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
-                           int grid, cudaStream_t stream) {
+cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                           const GemmArgs& args, int grid, cudaStream_t stream) {
+  constexpr int kSmem = Staging<SYM, EPI_WARPS>::kSmemBytes;
   // The dynamic shared-memory limit is raised once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -39,12 +40,12 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const Gem
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
     e = cudaFuncSetAttribute(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
   return launch_pdl(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS>, dim3(grid), dim3(Epi<EPI_WARPS>::kCtaThreads),
-                    kSmemBytes, stream, a, b, args);
+                    kSmem, stream, a, b, o, args);
 }
 
 }  // namespace mns

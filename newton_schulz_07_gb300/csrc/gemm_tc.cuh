@@ -57,6 +57,17 @@ namespace mns {
 
 constexpr int kBlockK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
+constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
+constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
+constexpr int kPipeBytes = kStages * kStageBytes;
+// Output staging: each epilogue warp stages 32 x 32 bf16 chunks (2 KB, rows
+// of 64 bytes, 64-byte TMA swizzle) that a bulk tensor store writes out.
+constexpr int kChunkBytes = 32 * 32 * 2;
+constexpr int kMnChunk = 64;                   // MN elements per 128-byte row
+constexpr int kMnChunkBytes = kMnChunk * kBlockK * 2;  // 8 KB
+
 // Epilogue warps: 4 or 8, i.e. one or two per TMEM lane quarter.  The
 // symmetric products (mirrored stores) always take 8; the update takes 8 when
 // its contraction is short (K <= 1024, little main-loop time per tile to hide
@@ -69,19 +80,29 @@ struct Epi {
   static constexpr int kCtaThreads = 64 + kThreads;  // + producer warp + MMA warp
   static constexpr int kChunksPerWarp = (kTileN / 32) / (kWarps / 4);
 };
-constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
-constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-constexpr int kMnChunk = 64;                   // MN elements per 128-byte row
-constexpr int kMnChunkBytes = kMnChunk * kBlockK * 2;  // 8 KB
+
+// Staging buffers per epilogue warp: symmetric products need two at once
+// (the chunk and its transpose); the update double-buffers with 4 warps and
+// single-buffers with 8 (shared-memory budget).
+template <bool SYM, int EPI_WARPS>
+struct Staging {
+  static constexpr int kBufs = SYM ? 2 : (EPI_WARPS == 4 ? 2 : 1);
+  static constexpr int kSmemBytes = kPipeBytes + EPI_WARPS * kBufs * kChunkBytes + 1024;  // + align
+};
+
+// Byte offset of element (row, col) of a 32 x 32 bf16 staging chunk: rows of
+// 64 bytes, 16-byte granule index XOR ((row >> 1) & 3) (the 64-byte TMA
+// swizzle), so that 32 lanes writing 32 different rows hit distinct banks.
+__device__ __forceinline__ uint32_t stage_off(int row, int col) {
+  const int g = (col >> 3) ^ ((row >> 1) & 3);
+  return static_cast<uint32_t>(row * 64 + g * 16 + (col & 7) * 2);
+}
 
 struct GemmArgs {
   TileSpace space;
   int M, N, K;        // output rows, output columns, contraction length
   int num_kb;         // ceil(K / kBlockK)
-  uint16_t* out;      // bf16 [batch][M][N], row stride ld
+  uint16_t* out;      // bf16 [batch][M][N], row stride ld (written through the output tensor map)
   const uint16_t* addend;  // same layout, or nullptr
   long long ld;
   long long bstride;
@@ -155,7 +176,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmArgs args) {
+               const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t tmem_base_sh;
@@ -188,6 +209,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
+    ptx::prefetch_tensormap(&tmOut);
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols);
@@ -324,6 +346,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const int c_begin = (e >> 2) * kChunksPerWarp;
     const int r_in_tile = q * 32 + lane;
     float* colc = colc_sh[SYM ? 0 : e];
+    constexpr int kBufs = Staging<SYM, EPI_WARPS>::kBufs;
+    const uint32_t stg = smem_base + kPipeBytes + static_cast<uint32_t>(e * kBufs * kChunkBytes);
     int buf = 0;
     uint32_t tphase = 0;
     for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
@@ -340,7 +364,6 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const long long gi = static_cast<long long>(I) * kTileM + r_in_tile;
       const int warp_row_max = I * kTileM + q * 32 + 31;
       const bool row_ok = gi < args.M;
-      uint16_t* outm = args.out + static_cast<long long>(b) * args.bstride;
       const uint16_t* addm =
           args.addend ? args.addend + static_cast<long long>(b) * args.bstride : nullptr;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -386,77 +409,101 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         uint32_t v[32];
         ptx::tmem_ld_32cols(t_lane + static_cast<uint32_t>((c_begin + cc) * 32), v);
         ptx::tmem_wait_ld();
-        if (row_ok) {
-          float f[32];
+        // Rows beyond M hold zeros (zero-filled operands); their stores are clipped.
+        float f[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
-          if (addm != nullptr) {
-            const uint32_t ws[16] = {av[0].x, av[0].y, av[0].z, av[0].w, av[1].x, av[1].y,
-                                     av[1].z, av[1].w, av[2].x, av[2].y, av[2].z, av[2].w,
-                                     av[3].x, av[3].y, av[3].z, av[3].w};
-            if (col_mode) {
-              const float4* cp = reinterpret_cast<const float4*>(colc + cc * 32);
+        for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
+        if (addm != nullptr) {
+          const uint32_t ws[16] = {av[0].x, av[0].y, av[0].z, av[0].w, av[1].x, av[1].y,
+                                   av[1].z, av[1].w, av[2].x, av[2].y, av[2].z, av[2].w,
+                                   av[3].x, av[3].y, av[3].z, av[3].w};
+          if (col_mode) {
+            const float4* cp = reinterpret_cast<const float4*>(colc + cc * 32);
 #pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                const float4 k4 = cp[h];
-                f[4 * h + 0] = fmaf(k4.x, detail::bf16_lo(ws[2 * h]), f[4 * h + 0]);
-                f[4 * h + 1] = fmaf(k4.y, detail::bf16_hi(ws[2 * h]), f[4 * h + 1]);
-                f[4 * h + 2] = fmaf(k4.z, detail::bf16_lo(ws[2 * h + 1]), f[4 * h + 2]);
-                f[4 * h + 3] = fmaf(k4.w, detail::bf16_hi(ws[2 * h + 1]), f[4 * h + 3]);
-              }
-            } else {
+            for (int h = 0; h < 8; ++h) {
+              const float4 k4 = cp[h];
+              f[4 * h + 0] = fmaf(k4.x, detail::bf16_lo(ws[2 * h]), f[4 * h + 0]);
+              f[4 * h + 1] = fmaf(k4.y, detail::bf16_hi(ws[2 * h]), f[4 * h + 1]);
+              f[4 * h + 2] = fmaf(k4.z, detail::bf16_lo(ws[2 * h + 1]), f[4 * h + 2]);
+              f[4 * h + 3] = fmaf(k4.w, detail::bf16_hi(ws[2 * h + 1]), f[4 * h + 3]);
+            }
+          } else {
 #pragma unroll
-              for (int h = 0; h < 16; ++h) {
-                f[2 * h] = fmaf(row_coef, detail::bf16_lo(ws[h]), f[2 * h]);
-                f[2 * h + 1] = fmaf(row_coef, detail::bf16_hi(ws[h]), f[2 * h + 1]);
-              }
+            for (int h = 0; h < 16; ++h) {
+              f[2 * h] = fmaf(row_coef, detail::bf16_lo(ws[h]), f[2 * h]);
+              f[2 * h + 1] = fmaf(row_coef, detail::bf16_hi(ws[h]), f[2 * h + 1]);
             }
           }
-          if (SYM && args.diag_out != nullptr && gi >= gj0 && gi < gj0 + 32) {
-            // The diagonal element goes to the fp32 side vector; 0 is stored.
-            float dval = 0.0f;
+        }
+        if (SYM && args.diag_out != nullptr && row_ok && gi >= gj0 && gi < gj0 + 32) {
+          // The diagonal element goes to the fp32 side vector; 0 is stored.
+          float dval = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (gj0 + j == gi) {
-                dval = f[j];
-                f[j] = 0.0f;
-              }
+          for (int j = 0; j < 32; ++j) {
+            if (gj0 + j == gi) {
+              dval = f[j];
+              f[j] = 0.0f;
             }
-            args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
           }
-          uint32_t hv[16];
+          args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
+        }
+        uint32_t hv[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
-          uint16_t* rowp = outm + gi * args.ld + gj0;
-          if (!SYM) {
-            uint4* dst = reinterpret_cast<uint4*>(rowp);
+        for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
+        // Stage the chunk in shared memory and write it with bulk tensor
+        // stores (rows beyond M or columns beyond N are clipped by the TMA).
+        const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
+        if (lane == 0) {
+          if (kBufs == 2 && !SYM) ptx::bulk_wait_read<1>();
+          else ptx::bulk_wait_read<0>();
+        }
+        __syncwarp();
+        if (!SYM) {
+          const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kChunkBytes);
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-              if (gj0 + 8 * g + 8 <= args.N)
-                dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
-          } else if (gj0 <= gi) {
-            if (gj0 + 31 <= gi && gj0 + 32 <= args.N) {
-              uint4* dst = reinterpret_cast<uint4*>(rowp);
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(d + stage_off(lane, 8 * g), hv[4 * g], hv[4 * g + 1], hv[4 * g + 2],
+                              hv[4 * g + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
+            ptx::bulk_commit();
+          }
+        } else if (gj0 < R0) {
+          // Below the diagonal: the chunk at (R0, gj0) and its transpose at (gj0, R0).
+          const uint32_t d = stg;
+          const uint32_t tr = stg + kChunkBytes;
 #pragma unroll
-              for (int g = 0; g < 4; ++g)
-                dst[g] = make_uint4(hv[4 * g], hv[4 * g + 1], hv[4 * g + 2], hv[4 * g + 3]);
-            } else {
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(d + stage_off(lane, 8 * g), hv[4 * g], hv[4 * g + 1], hv[4 * g + 2],
+                              hv[4 * g + 3]);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const long long gj = gj0 + j;
-                if (gj <= gi && gj < args.N)
-                  rowp[j] = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-              }
-            }
-            // Mirror: (gj, gi) for gj < gi.  Lanes hold consecutive gi, so each
-            // store instruction writes 64 contiguous bytes of row gj.
+          for (int j = 0; j < 32; ++j)
+            ptx::st_shared_u16(tr + stage_off(j, lane),
+                               static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
+            ptx::tma_store_3d(&tmOut, tr, R0, gj0, b);
+            ptx::bulk_commit();
+          }
+        } else {
+          // Diagonal 32 x 32 block (gj0 == R0): entry (r, j) takes the value
+          // computed at (max(r, j), min(r, j)), so the block is bit-symmetric.
+          const uint32_t d = stg;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const long long gj = gj0 + j;
-              if (gj < gi && gj < args.N)
-                outm[gj * args.ld + gi] =
-                    static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-            }
+          for (int j = 0; j < 32; ++j) {
+            const uint16_t hj = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+            if (j <= lane) ptx::st_shared_u16(d + stage_off(lane, j), hj);
+            if (j < lane) ptx::st_shared_u16(d + stage_off(j, lane), hj);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
+            ptx::bulk_commit();
           }
         }
 #pragma unroll
@@ -467,6 +514,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       buf ^= 1;
       if (buf == 0) tphase ^= 1u;
     }
+    // Staging buffers stay valid until every bulk store of this warp is done.
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();

@@ -145,9 +145,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D bf16 map over a stack [batch][rows][inner] (inner contiguous) with a
-// box of box_inner x box_rows x 1 and 128-byte swizzle.
+// box of box_inner x box_rows x 1; 128-byte swizzle for operand tiles, 64-byte
+// swizzle for the 32 x 32 output chunks.
 bool make_map(CUtensorMap* map, const void* base, long long inner, long long rows,
-              long long batch, int box_inner, int box_rows) {
+              long long batch, int box_inner, int box_rows,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
@@ -158,7 +160,7 @@ bool make_map(CUtensorMap* map, const void* base, long long inner, long long row
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
       fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -183,6 +185,11 @@ GemmArgs base_args(int sym, long long batch, long long M, long long N, long long
   return a;
 }
 
+// Output map: [batch][M][N] bf16, 32 x 32 boxes, 64-byte swizzle.
+bool make_out_map(CUtensorMap* map, const void* base, long long M, long long N, long long batch) {
+  return make_map(map, base, N, M, batch, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 int grid_for(const GemmArgs& a, int sms) {
   const long long g = a.space.total < sms ? a.space.total : sms;
   return static_cast<int>(g < 1 ? 1 : g);
@@ -192,26 +199,28 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? MUON_NS_OK : MUON_NS_ER
 
 int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, int* err, int sms,
              cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   GemmArgs a = base_args(1, p.batch, p.m, p.m, p.n, err);
   a.out = A;
+  if (!make_out_map(&to, A, p.m, p.m, p.batch)) return MUON_NS_ERR_CUDA;
   if (!p.T) {
     // X [batch][m][n]: rows of X are the K-major operand rows.
     if (!make_map(&ta, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
         !make_map(&tb, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileN))
       return MUON_NS_ERR_CUDA;
-    return to_status(mns::launch_sym_kk(ta, tb, a, grid_for(a, sms), st));
+    return to_status(mns::launch_sym_kk(ta, tb, to, a, grid_for(a, sms), st));
   }
   // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
   if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kMnChunk, mns::kBlockK)) return MUON_NS_ERR_CUDA;
-  return to_status(mns::launch_sym_mnmn(ta, ta, a, grid_for(a, sms), st));
+  return to_status(mns::launch_sym_mnmn(ta, ta, to, a, grid_for(a, sms), st));
 }
 
 int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float* diag, float b,
              float c, int* err, int sms, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if (!make_map(&ta, A, m, m, batch, mns::kBlockK, mns::kTileM) ||
-      !make_map(&tb, A, m, m, batch, mns::kBlockK, mns::kTileN))
+      !make_map(&tb, A, m, m, batch, mns::kBlockK, mns::kTileN) ||
+      !make_out_map(&to, B, m, m, batch))
     return MUON_NS_ERR_CUDA;
   GemmArgs a = base_args(1, batch, m, m, m, err);
   a.out = B;
@@ -219,12 +228,13 @@ int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float
   a.alpha = c;
   a.beta = b;
   a.diag_out = diag;
-  return to_status(mns::launch_sym_kk(ta, tb, a, grid_for(a, sms), st));
+  return to_status(mns::launch_sym_kk(ta, tb, to, a, grid_for(a, sms), st));
 }
 
 int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const float* diag,
                uint16_t* Xn, float alpha_x, int* err, int sms, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
+  if (!make_out_map(&to, Xn, p.T ? p.n : p.m, p.T ? p.m : p.n, p.batch)) return MUON_NS_ERR_CUDA;
   if (!p.T) {
     // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
     if (!make_map(&ta, B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
@@ -236,7 +246,7 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const flo
     a.beta = alpha_x;
     a.diag_in = diag;  // (a + D_i) scales row i of X
     a.diag_per_col = 0;
-    return to_status(mns::launch_full_kmn(ta, tb, a, grid_for(a, sms), st));
+    return to_status(mns::launch_full_kmn(ta, tb, to, a, grid_for(a, sms), st));
   }
   // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
   if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kBlockK, mns::kTileM) ||
@@ -248,7 +258,7 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const flo
   a.beta = alpha_x;
   a.diag_in = diag;  // Y D: (a + D_j) scales column j of Y
   a.diag_per_col = 1;
-  return to_status(mns::launch_full_kk(ta, tb, a, grid_for(a, sms), st));
+  return to_status(mns::launch_full_kk(ta, tb, to, a, grid_for(a, sms), st));
 }
 
 int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* X, float eps,

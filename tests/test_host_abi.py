@@ -215,3 +215,31 @@ def test_symmetric_epilogue_writes_each_element_once(m):
 @pytest.mark.parametrize("M,N", [(8, 8), (136, 264), (400, 1000)])
 def test_full_epilogue_writes_each_element_once(M, N):
     assert np.all(_epilogue_writes(1, M, N, tiles(1, 1, M, N)) == 1)
+
+
+def _chunk_store_writes(m, ts, warps_per_quarter=2):
+    """Model of the symmetric epilogue's bulk stores: per 32-row warp block and
+    32-column chunk, the chunk (below the diagonal) plus its transpose, or the
+    symmetrised diagonal block; counts writes per 32 x 32 block."""
+    nb = -(-m // 32)
+    count = np.zeros((nb, nb), dtype=np.int32)
+    for _, I, J in ts:
+        for q in range(4):
+            R0 = I * TILE_M + q * 32
+            if R0 >= m:
+                continue  # all rows clipped
+            for cc in range(TILE_N // 32):
+                gj0 = J * TILE_N + cc * 32
+                if gj0 >= m or gj0 > R0 + 31:
+                    break
+                if gj0 < R0:
+                    count[R0 // 32, gj0 // 32] += 1
+                    count[gj0 // 32, R0 // 32] += 1
+                else:
+                    count[R0 // 32, R0 // 32] += 1
+    return count
+
+
+@pytest.mark.parametrize("m", [8, 136, 256, 392, 640, 1000, 1536])
+def test_symmetric_bulk_stores_write_each_block_once(m):
+    assert np.all(_chunk_store_writes(m, tiles(0, 1, m, m)) == 1)
