@@ -88,7 +88,7 @@ def flop_counts(w, steps=5):
         "gram": b * m * (m + 1) * n,
         "poly": b * m * m * (m + 1),
         "update": b * 2 * m * m * n,
-        "normalize_bytes": b * 6.0 * w.rows * w.cols,
+        "norm_bytes": b * 2.0 * w.rows * w.cols,
         "dense_call": w.dense_flops(steps),
         "useful_call": w.useful_flops(steps),
     }
@@ -308,41 +308,46 @@ def main():
     ms = max_over_ranks(ms_local)
     dev_err = ns.read_error(ws)
 
-    # Per-kernel breakdown: the same kernels through the per-step entry points,
-    # CUDA events on the launching stream between launches.
+    # Per-kernel breakdown: the same kernels in the same launch configuration
+    # as muon_ns_ws, through the per-step entry points, with CUDA events on the
+    # launching stream between launches.  Step 1 reads G and applies the
+    # per-matrix scale in its epilogues, as the whole call does.
     nb = min(args.steps, 20)
-    names = ["normalize", "gram", "poly", "update"]
+    names = ["norm", "gram", "poly", "update"]
     acc = {k: 0.0 for k in names}
     a_buf = torch.empty((w.batch, w.m, w.m), dtype=torch.bfloat16, device=dev)
     b_buf = torch.empty_like(a_buf)
     x_bufs = [torch.empty_like(G), torch.empty_like(G)]
     err_word = torch.zeros(1, dtype=torch.int32, device=dev)
     d_buf = torch.empty((w.batch, w.m), dtype=torch.float32, device=dev)
+    n_off, n_bytes = ns.workspace_region(w.batch, w.rows, w.cols, 2)
+    norms_t = ws[n_off:n_off + n_bytes].view(torch.float32)
     a, b, c = ns.DEFAULT_COEFFS
     for it in range(nb + 2):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
         ev[0].record(stream)
-        ns.muon_ns_normalize(G, ws, X=x_bufs[0])
+        ns.muon_ns_normalize(G, ws, norms_only=True)
         ev[1].record(stream)
-        cur = 0
+        src, cur = G, 0
         for s in range(5):
-            ns.muon_ns_gram(x_bufs[cur], A=a_buf, device_error=err_word)
+            ns.muon_ns_gram(src, A=a_buf, device_error=err_word, norms=norms_t if s == 0 else None)
             ev[2 + 3 * s].record(stream)
             ns.muon_ns_poly(a_buf, b, c, B=b_buf, diag=d_buf, device_error=err_word)
             ev[3 + 3 * s].record(stream)
-            ns.muon_ns_update(x_bufs[cur], b_buf, a, Xn=x_bufs[1 - cur], diag=d_buf, device_error=err_word)
+            ns.muon_ns_update(src, b_buf, a, Xn=x_bufs[cur], diag=d_buf, device_error=err_word,
+                              norms=norms_t if s == 0 else None)
             ev[4 + 3 * s].record(stream)
-            cur = 1 - cur
+            src, cur = x_bufs[cur], 1 - cur
         torch.cuda.synchronize()
         if it < 2:
             continue
-        acc["normalize"] += ev[0].elapsed_time(ev[1])
+        acc["norm"] += ev[0].elapsed_time(ev[1])
         for s in range(5):
             acc["gram"] += ev[1 + 3 * s].elapsed_time(ev[2 + 3 * s]) / 5
             acc["poly"] += ev[2 + 3 * s].elapsed_time(ev[3 + 3 * s]) / 5
             acc["update"] += ev[3 + 3 * s].elapsed_time(ev[4 + 3 * s]) / 5
     per_launch_ms = {k: v / nb for k, v in acc.items()}
-    share = {"normalize": per_launch_ms["normalize"]}
+    share = {"norm": per_launch_ms["norm"]}
     for k in ("gram", "poly", "update"):
         share[k] = 5 * per_launch_ms[k]
     dominant = max(("gram", "poly", "update"), key=lambda k: share[k])
@@ -356,12 +361,12 @@ def main():
                 "traffic": traffic,
                 "algorithmic_flops_per_launch": fl[dominant],
                 "avg_launch_ms": per_launch_ms[dominant]}
-    norm_gbs = fl["normalize_bytes"] / (per_launch_ms["normalize"] * 1e-3) / 1e9
+    norm_gbs = fl["norm_bytes"] / (per_launch_ms["norm"] * 1e-3) / 1e9
     breakdown = {
         "per_launch_ms": per_launch_ms,
         "per_call_ms": share,
-        "normalize_hbm": {"achieved_gbs": norm_gbs, "peak_gbs": peaks["hbm_gbs"],
-                          "frac": norm_gbs / peaks["hbm_gbs"], "bytes_per_call": fl["normalize_bytes"]},
+        "norm_hbm": {"achieved_gbs": norm_gbs, "peak_gbs": peaks["hbm_gbs"],
+                     "frac": norm_gbs / peaks["hbm_gbs"], "bytes_per_call": fl["norm_bytes"]},
         "tensor_tflops_useful": {k: fl[k] / (per_launch_ms[k] * 1e-3) / 1e12 for k in ("gram", "poly", "update")},
     }
 

@@ -124,8 +124,12 @@ int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* 
  *   workspace  device, >= muon_ns_workspace_size() bytes, 256-byte aligned,
  *              caller-owned.  Nothing is allocated and nothing synchronises,
  *              so the call can be captured in a CUDA graph.
- * Kernel launches per call: 2 + 3 * steps (norm, scale, then per step the
- * Gram, polynomial and update kernels). */
+ * Kernel launches per call: 1 + 3 * steps (the norm, then per step the Gram,
+ * polynomial and update kernels); 2 when steps == 0 (norm and scale).  The
+ * first step reads G itself and applies s = 1 / (||G||_F + eps) in its
+ * epilogues (A0 = s^2 G G^T, X1 = s (a + D) G + s O G), so no scaled copy of G
+ * is made and X0 is never rounded to bf16.  In place with an odd step count
+ * the result is copied once from the workspace into out at the end. */
 int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
                const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
@@ -153,18 +157,21 @@ int muon_ns_cached_error(int device, int* device_error);
 
 /* X = bf16(G * (1 / (||G_k||_F + eps))) per matrix, in the input orientation,
  * and norms[k] = ||G_k||_F (fp32, sum of squares accumulated in fp32 in a
- * fixed order, so the result is the same for a matrix alone or in any stack).
- * `workspace` as for muon_ns_ws (only its header and norm regions are used).
- * X == G is allowed.  Two kernel launches. */
+ * fixed order, so the result is the same for a matrix alone or in any stack)
+ * in the workspace's MUON_NS_WS_NORMS region.  `workspace` as for muon_ns_ws
+ * (only its header and norm regions are used).  X == G is allowed; X == NULL
+ * computes the norms only (one launch instead of two). */
 int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols, float eps,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Gram matrix of the internal orientation, bf16 [batch][m][m], m = min(rows, cols):
  *   rows <= cols:  A = X X^T        rows > cols:  A = X^T X
  * Only lower-triangle tiles are computed; each value is written to (i, j) and
- * (j, i), so A is bit-symmetric.  fp32 accumulation, one rounding to bf16. */
+ * (j, i), so A is bit-symmetric.  fp32 accumulation, one rounding to bf16.
+ *   norms  NULL, or device fp32 [batch]: then X is taken as unscaled and the
+ *          Gram of X_k / (norms[k] + eps) is computed (the first NS step). */
 int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
-                 int* device_error, cudaStream_t stream);
+                 const float* norms, float eps, int* device_error, cudaStream_t stream);
 
 /* B = b A + c (A A) for a bit-symmetric A, bf16 [batch][m][m].  A A is formed
  * as A A^T (equal for a bit-symmetric A) over lower-triangle tiles; the
@@ -185,9 +192,12 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m
  * fp32 epilogue reading X.  Xn must not overlap X or B.
  *   diag  NULL, or the fp32 diagonal written by muon_ns_poly (then B's stored
  *         diagonal must be zero): the epilogue applies (a + diag_i) to X in
- *         fp32, row i for rows <= cols, column i for rows > cols. */
+ *         fp32, row i for rows <= cols, column i for rows > cols.
+ *   norms NULL, or device fp32 [batch]: then X is taken as unscaled and the
+ *         update of X_k / (norms[k] + eps) is computed (the first NS step). */
 int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
-                   int batch, int rows, int cols, float a, int* device_error, cudaStream_t stream);
+                   int batch, int rows, int cols, float a, const float* norms, float eps,
+                   int* device_error, cudaStream_t stream);
 
 /* X = bf16(G * (1 / (||G_k||_F + eps))) exactly as muon_ns_normalize(), for
  * callers that cannot allocate device memory (plugins handed only their
@@ -213,7 +223,7 @@ int muon_ns_normalize_static(const muon_bf16* G, muon_bf16* X, int batch, int ro
  * Host-only helpers (no GPU needed).
  * ------------------------------------------------------------------------- */
 
-/* Kernel launches made by one muon_ns_ws() call: 2 + 3 * steps. */
+/* Kernel launches made by one muon_ns_ws() call: 1 + 3 * steps (2 if steps == 0). */
 int muon_ns_launches_per_call(int steps);
 
 /* Persistent tile scheduler of the tensor-core kernels.  kind 0 = lower

@@ -39,9 +39,9 @@ SIGNATURES = {
     "muon_ns_cached_error": (_c_int, [_c_int, _pi]),
     "muon_ns_normalize": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_normalize_static": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp]),
-    "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_f, _vp, _vp]),
     "muon_ns_poly": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
-    "muon_ns_update": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _vp]),
+    "muon_ns_update": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_f, _vp, _vp]),
     "muon_ns_launches_per_call": (_c_int, [_c_int]),
     "muon_ns_tile_count": (_c_ll, [_c_int, _c_int, _c_int, _c_int]),
     "muon_ns_tile_coords": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_ll, _pi, _pi, _pi]),

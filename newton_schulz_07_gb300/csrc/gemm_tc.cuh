@@ -115,6 +115,13 @@ struct GemmArgs {
   float* diag_out;
   const float* diag_in;
   int diag_per_col;
+  // Unscaled operands (optional): with norms != nullptr the operands are the
+  // raw G of each matrix and s = 1 / (norms[b] + eps) is applied in the
+  // epilogue, so the first step needs no scaled copy of G:
+  //   SYM (Gram)      out = alpha s^2 acc
+  //   FULL (update)   out = alpha s acc + (beta + diag) s addend
+  const float* norms;
+  float eps;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -370,9 +377,13 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
                               static_cast<uint32_t>(buf * kTileN);
       const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
       // Addend coefficient: per row (row-indexed diagonal or none) ...
+      float mscale = 1.0f;  // per-matrix scale of unscaled operands
+      if (args.norms != nullptr) mscale = 1.0f / (__ldg(args.norms + b) + args.eps);
+      const float alpha_t = SYM ? args.alpha * (mscale * mscale) : args.alpha * mscale;
       float row_coef = args.beta;
       if (!SYM && args.diag_in != nullptr && !args.diag_per_col && row_ok)
         row_coef += __ldg(args.diag_in + static_cast<long long>(b) * args.M + gi);
+      row_coef *= mscale;
       // ... or per column, staged in shared memory for this warp's columns.
       const bool col_mode = !SYM && args.diag_in != nullptr && args.diag_per_col;
       if (col_mode) {
@@ -380,7 +391,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         for (int v = 0; v < kChunksPerWarp; ++v) {
           const int col = col_base + v * 32 + lane;
           colc[v * 32 + lane] =
-              args.beta + (col < args.N ? __ldg(args.diag_in + static_cast<long long>(b) * args.N + col) : 0.0f);
+              (args.beta + (col < args.N ? __ldg(args.diag_in + static_cast<long long>(b) * args.N + col) : 0.0f)) *
+              mscale;
         }
         __syncwarp();
       }
@@ -412,7 +424,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // Rows beyond M hold zeros (zero-filled operands); their stores are clipped.
         float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = args.alpha * __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) f[j] = alpha_t * __uint_as_float(v[j]);
         if (addm != nullptr) {
           const uint32_t ws[16] = {av[0].x, av[0].y, av[0].z, av[0].w, av[1].x, av[1].y,
                                    av[1].z, av[1].w, av[2].x, av[2].y, av[2].z, av[2].w,

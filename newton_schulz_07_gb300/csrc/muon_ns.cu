@@ -197,11 +197,13 @@ int grid_for(const GemmArgs& a, int sms) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? MUON_NS_OK : MUON_NS_ERR_CUDA; }
 
-int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, int* err, int sms,
-             cudaStream_t st) {
+int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, const float* norms, float eps,
+             int* err, int sms, cudaStream_t st) {
   CUtensorMap ta, tb, to;
   GemmArgs a = base_args(1, p.batch, p.m, p.m, p.n, err);
   a.out = A;
+  a.norms = norms;
+  a.eps = eps;
   if (!make_out_map(&to, A, p.m, p.m, p.batch)) return MUON_NS_ERR_CUDA;
   if (!p.T) {
     // X [batch][m][n]: rows of X are the K-major operand rows.
@@ -232,7 +234,8 @@ int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float
 }
 
 int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const float* diag,
-               uint16_t* Xn, float alpha_x, int* err, int sms, cudaStream_t st) {
+               uint16_t* Xn, float alpha_x, const float* norms, float eps, int* err, int sms,
+               cudaStream_t st) {
   CUtensorMap ta, tb, to;
   if (!make_out_map(&to, Xn, p.T ? p.n : p.m, p.T ? p.m : p.n, p.batch)) return MUON_NS_ERR_CUDA;
   if (!p.T) {
@@ -246,6 +249,8 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const flo
     a.beta = alpha_x;
     a.diag_in = diag;  // (a + D_i) scales row i of X
     a.diag_per_col = 0;
+    a.norms = norms;
+    a.eps = eps;
     return to_status(mns::launch_full_kmn(ta, tb, to, a, grid_for(a, sms), st));
   }
   // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
@@ -258,6 +263,8 @@ int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const flo
   a.beta = alpha_x;
   a.diag_in = diag;  // Y D: (a + D_j) scales column j of Y
   a.diag_per_col = 1;
+  a.norms = norms;
+  a.eps = eps;
   return to_status(mns::launch_full_kk(ta, tb, to, a, grid_for(a, sms), st));
 }
 
@@ -273,6 +280,7 @@ int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t
                       reinterpret_cast<unsigned int*>(ws + L.tickets),
                       reinterpret_cast<float*>(ws + L.norms)) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
+  if (X == nullptr) return MUON_NS_OK;  // norms only
   if (mns::launch_pdl(mns::ns_scale, grid, dim3(mns::kNormThreads), 0, st,
                       reinterpret_cast<const uint4*>(G), reinterpret_cast<uint4*>(X), vec,
                       reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
@@ -288,16 +296,33 @@ int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, 
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
   uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
   float* D = reinterpret_cast<float*>(ws + L.diag);
-  uint16_t* cur = (steps % 2 == 1) ? wsx : out;
-  int s = run_normalize(p, L, G, cur, eps, ws, st);
+  const float* norms = reinterpret_cast<const float*>(ws + L.norms);
+  if (steps == 0) return run_normalize(p, L, G, out, eps, ws, st);
+  // Norms only; the first step reads G itself and applies s = 1/(norm + eps)
+  // in its epilogues (A0 = s^2 G G^T, X1 = s O G + s (a + D) G), so no scaled
+  // copy of G is written or read.
+  int s = run_normalize(p, L, G, nullptr, eps, ws, st);
   if (s != MUON_NS_OK) return s;
-  for (int k = 0; k < steps; ++k) {
+  // Iterates alternate between the workspace and `out` so that the last one
+  // lands in `out`; in place (out == G) the first iterate must not overwrite
+  // G while step 1 still reads it, so it goes to the workspace and an odd step
+  // count ends with one copy.
+  const bool in_place = out == G;
+  uint16_t* cur = (in_place || steps % 2 == 0) ? wsx : out;
+  if ((s = run_gram(p, G, A, norms, eps, err, sms, st)) != MUON_NS_OK) return s;
+  if ((s = run_poly(p.batch, p.m, A, B, D, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
+  if ((s = run_update(p, G, B, D, cur, abc[0], norms, eps, err, sms, st)) != MUON_NS_OK) return s;
+  for (int k = 1; k < steps; ++k) {
     uint16_t* nxt = (cur == out) ? wsx : out;
-    if ((s = run_gram(p, cur, A, err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_gram(p, cur, A, nullptr, 0.0f, err, sms, st)) != MUON_NS_OK) return s;
     if ((s = run_poly(p.batch, p.m, A, B, D, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-    if ((s = run_update(p, cur, B, D, nxt, abc[0], err, sms, st)) != MUON_NS_OK) return s;
+    if ((s = run_update(p, cur, B, D, nxt, abc[0], nullptr, 0.0f, err, sms, st)) != MUON_NS_OK)
+      return s;
     cur = nxt;
   }
+  if (cur != out &&
+      cudaMemcpyAsync(out, cur, L.x_bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
   return MUON_NS_OK;
 }
 
@@ -492,7 +517,7 @@ int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int
   if (s != MUON_NS_OK) return s;
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
-  if (!G || !X) return MUON_NS_ERR_INVALID_ARG;
+  if (!G) return MUON_NS_ERR_INVALID_ARG;
   if (!aligned16(G) || !aligned16(X)) return MUON_NS_ERR_ALIGNMENT;
   const Layout L = make_layout(p);
   if (!workspace || workspace_bytes < L.total) return MUON_NS_ERR_WORKSPACE;
@@ -503,17 +528,18 @@ int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int
 }
 
 int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
-                 int* device_error, cudaStream_t stream) {
+                 const float* norms, float eps, int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, rows, cols, &p, &empty);
   if (s != MUON_NS_OK) return s;
   if (empty) return MUON_NS_OK;
   if (!X || !A) return MUON_NS_ERR_INVALID_ARG;
+  if (norms && (!(eps >= 0.0f) || !std::isfinite(eps))) return MUON_NS_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(A)) return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_gram(p, X, A, device_error, d.sms, stream);
+  return run_gram(p, X, A, norms, eps, device_error, d.sms, stream);
 }
 
 int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
@@ -532,22 +558,26 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m
 }
 
 int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
-                   int batch, int rows, int cols, float a, int* device_error, cudaStream_t stream) {
+                   int batch, int rows, int cols, float a, const float* norms, float eps,
+                   int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, rows, cols, &p, &empty);
   if (s != MUON_NS_OK) return s;
   if (!std::isfinite(a)) return MUON_NS_ERR_INVALID_ARG;
+  if (norms && (!(eps >= 0.0f) || !std::isfinite(eps))) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!X || !B || !Xn || Xn == X || Xn == B) return MUON_NS_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(B) || !aligned16(Xn) || !aligned16(diag))
     return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_update(p, X, B, diag, Xn, a, device_error, d.sms, stream);
+  return run_update(p, X, B, diag, Xn, a, norms, eps, device_error, d.sms, stream);
 }
 
-int muon_ns_launches_per_call(int steps) { return steps < 0 ? -1 : 2 + 3 * steps; }
+int muon_ns_launches_per_call(int steps) {
+  return steps < 0 ? -1 : (steps == 0 ? 2 : 1 + 3 * steps);
+}
 
 long long muon_ns_tile_count(int kind, int batch, int M, int N) {
   if ((kind != 0 && kind != 1) || batch < 0 || M < 0 || N < 0) return -1;

@@ -91,25 +91,33 @@ def muon_ns(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float =
 
 
 def muon_ns_normalize(G: torch.Tensor, workspace: torch.Tensor, eps: float = DEFAULT_EPS,
-                      X: torch.Tensor | None = None) -> torch.Tensor:
+                      X: torch.Tensor | None = None, norms_only: bool = False):
+    """X = G / (||G||_F + eps); the norms go to the workspace's NORMS region.
+    With norms_only=True only the norm kernel runs and None is returned."""
     _check_bf16(G, "G")
     b, r, c = _shape3(G)
-    X = torch.empty_like(G) if X is None else X
+    if norms_only:
+        X = None
+    elif X is None:
+        X = torch.empty_like(G)
     with torch.cuda.device(G.device):
         _lib.check(_lib.lib().muon_ns_normalize(_ptr(G), _ptr(X), b, r, c, float(eps), _ptr(workspace),
                                                 workspace.numel(), _stream(G.device)), "muon_ns_normalize")
     return X
 
 
-def muon_ns_gram(X: torch.Tensor, A: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+def muon_ns_gram(X: torch.Tensor, A: torch.Tensor | None = None, device_error: torch.Tensor | None = None,
+                 norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS):
+    """A = X X^T (X^T X for tall X); with `norms` (fp32 [batch]) X is unscaled
+    and the Gram of X / (norms + eps) is computed."""
     _check_bf16(X, "X")
     b, r, c = _shape3(X)
     m = min(r, c)
     if A is None:
         A = torch.empty((b, m, m) if X.dim() == 3 else (m, m), dtype=torch.bfloat16, device=X.device)
     with torch.cuda.device(X.device):
-        _lib.check(_lib.lib().muon_ns_gram(_ptr(X), _ptr(A), b, r, c, _ptr(device_error), _stream(X.device)),
-                   "muon_ns_gram")
+        _lib.check(_lib.lib().muon_ns_gram(_ptr(X), _ptr(A), b, r, c, _ptr(norms), float(eps), _ptr(device_error),
+                                           _stream(X.device)), "muon_ns_gram")
     return A
 
 
@@ -131,7 +139,8 @@ def muon_ns_poly(A: torch.Tensor, b: float, c: float, B: torch.Tensor | None = N
 
 
 def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor | None = None,
-                   diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+                   diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None,
+                   norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS):
     """X' = a X + B X (X' = a X + X B for tall X).  With `diag` from
     muon_ns_poly, B = diag(D) + B_stored."""
     _check_bf16(X, "X")
@@ -143,7 +152,8 @@ def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor 
     Xn = torch.empty_like(X) if Xn is None else Xn
     with torch.cuda.device(X.device):
         _lib.check(_lib.lib().muon_ns_update(_ptr(X), _ptr(B), _ptr(diag), _ptr(Xn), bt, r, c, float(a),
-                                             _ptr(device_error), _stream(X.device)), "muon_ns_update")
+                                             _ptr(norms), float(eps), _ptr(device_error), _stream(X.device)),
+                   "muon_ns_update")
     return Xn
 
 

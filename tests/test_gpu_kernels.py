@@ -123,3 +123,54 @@ def test_device_error_word_stays_clear():
     ns.muon_ns_update(X, B, 3.4445, diag=D, device_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("shape", [(3, 136, 264), (2, 264, 136), (1, 392, 200)])
+def test_normalize_norms_only(shape):
+    bits = random_bits(shape, seed=5 + sum(shape), scale=0.3)
+    ws = ns.alloc_workspace(*shape)
+    assert ns.muon_ns_normalize(to_dev(bits), ws, norms_only=True) is None
+    off, nb = ns.workspace_region(*shape, ns._lib.WS_NORMS)
+    norms = ws[off:off + nb].view(torch.float32).cpu().numpy()
+    g = f64(bits)
+    for k in range(shape[0]):
+        assert abs(norms[k] - oracle.frobenius_norm(g[k])) <= 1e-5 * oracle.frobenius_norm(g[k])
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_gram_of_unscaled_input(shape):
+    # The first NS step: X is the raw G and the Gram of G / (norm + eps) is formed.
+    bits = random_bits(shape, seed=17 + sum(shape), scale=3.0)
+    norms = torch.from_numpy(np.array([oracle.frobenius_norm(m) for m in f64(bits)], dtype=np.float32)).cuda()
+    A = ns.muon_ns_gram(to_dev(bits), norms=norms, eps=1e-7)
+    torch.cuda.synchronize()
+    a = to_bits(A)
+    np.testing.assert_array_equal(a, np.swapaxes(a, 1, 2))
+    x = f64(bits)
+    nu = norms.cpu().numpy().astype(np.float64)
+    ref = np.stack([gram_ref(x[k] / (nu[k] + 1e-7)) for k in range(shape[0])])
+    assert max(per_matrix_rel(f64(a), ref)) <= KERNEL_TOL
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_update_of_unscaled_input(shape):
+    batch, r, c = shape
+    m = min(r, c)
+    xbits = random_bits(shape, seed=19 + r, scale=2.0)
+    bbits = symmetric_bits(batch, m, seed=23 + c, scale=0.05)
+    idx = np.arange(m)
+    dvals = np.random.default_rng(r * c).uniform(-3.0, 1.0, size=(batch, m)).astype(np.float32)
+    bbits[:, idx, idx] = 0
+    B = f64(bbits)
+    B[:, idx, idx] = dvals
+    x = f64(xbits)
+    nu = np.array([oracle.frobenius_norm(x[k]) for k in range(batch)], dtype=np.float32)
+    a = 3.4445
+    Xn = ns.muon_ns_update(to_dev(xbits), to_dev(bbits), a, diag=torch.from_numpy(dvals).cuda(),
+                           norms=torch.from_numpy(nu).cuda(), eps=1e-7)
+    torch.cuda.synchronize()
+    ref = []
+    for k in range(batch):
+        xs = x[k] / (float(nu[k]) + 1e-7)
+        ref.append(oracle.update(xs, B[k], a) if r <= c else oracle.update(xs.T, B[k], a).T)
+    assert max(per_matrix_rel(to_f64(Xn), np.stack(ref))) <= KERNEL_TOL

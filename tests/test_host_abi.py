@@ -48,7 +48,7 @@ def test_version_and_status_strings():
 
 def test_launch_count():
     L = _lib.lib()
-    assert [L.muon_ns_launches_per_call(s) for s in (0, 1, 5)] == [2, 5, 17]
+    assert [L.muon_ns_launches_per_call(s) for s in (0, 1, 5)] == [2, 4, 16]
     assert L.muon_ns_launches_per_call(-1) == -1
 
 
@@ -126,13 +126,16 @@ def test_argument_validation_codes():
     assert _call_ws(G=0, out=0, ws=0, batch=0) == _lib.OK
     assert _call_ws(G=0, out=0, ws=0, rows=0) == _lib.OK
     L = _lib.lib()
-    assert L.muon_ns_gram(None, None, 1, 16, 12, None, None) == _lib.ERR_ALIGNMENT
-    assert L.muon_ns_gram(None, None, 1, 16, 16, None, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_gram(None, None, 1, 16, 12, None, 0.0, None, None) == _lib.ERR_ALIGNMENT
+    assert L.muon_ns_gram(None, None, 1, 16, 16, None, 0.0, None, None) == _lib.ERR_INVALID_ARG
+    p8 = ctypes.c_void_p(8192)
+    assert L.muon_ns_gram(ctypes.c_void_p(4096), p8, 1, 16, 16, p8, -1.0, None, None) == _lib.ERR_INVALID_ARG
     p = ctypes.c_void_p(4096)
     assert L.muon_ns_poly(p, p, None, 1, 16, 1.0, 1.0, None, None) == _lib.ERR_INVALID_ARG  # B == A
     assert L.muon_ns_poly(p, ctypes.c_void_p(8192), ctypes.c_void_p(12), 1, 16, 1.0, 1.0, None,
                           None) == _lib.ERR_ALIGNMENT  # diag not 16-byte aligned
-    assert L.muon_ns_update(p, ctypes.c_void_p(8192), None, p, 1, 16, 16, 1.0, None, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_update(p, ctypes.c_void_p(8192), None, p, 1, 16, 16, 1.0, None, 0.0, None,
+                            None) == _lib.ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
