@@ -4,16 +4,14 @@
 
 namespace mns {
 
-cudaError_t launch_full_kmn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmArgs& args,
-                            int grid, cudaStream_t stream) {
-  return args.K <= 1024 ? launch_tc_gemm<false, true, false, 8>(a, b, o, args, grid, stream)
-                        : launch_tc_gemm<false, true, false, 4>(a, b, o, args, grid, stream);
+cudaError_t launch_full_kmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream) {
+  return max_k <= 1024 ? launch_tc_gemm<false, true, false, 8>(p, grid, stream)
+                       : launch_tc_gemm<false, true, false, 4>(p, grid, stream);
 }
 
-cudaError_t launch_full_kk(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmArgs& args,
-                           int grid, cudaStream_t stream) {
-  return args.K <= 1024 ? launch_tc_gemm<false, false, false, 8>(a, b, o, args, grid, stream)
-                        : launch_tc_gemm<false, false, false, 4>(a, b, o, args, grid, stream);
+cudaError_t launch_full_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream) {
+  return max_k <= 1024 ? launch_tc_gemm<false, false, false, 8>(p, grid, stream)
+                       : launch_tc_gemm<false, false, false, 4>(p, grid, stream);
 }
 
 }  // namespace mns

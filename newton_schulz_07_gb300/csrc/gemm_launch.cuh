@@ -29,8 +29,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
-cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                           const GemmArgs& args, int grid, cudaStream_t stream) {
+cudaError_t launch_tc_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Staging<SYM, EPI_WARPS>::kSmemBytes;
   // The dynamic shared-memory limit is raised once per device.
   static std::atomic<unsigned long long> configured{0};
@@ -45,7 +44,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUt
     configured.fetch_or(bit);
   }
   return launch_pdl(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS>, dim3(grid), dim3(Epi<EPI_WARPS>::kCtaThreads),
-                    kSmem, stream, a, b, o, args);
+                    kSmem, stream, p);
 }
 
 }  // namespace mns

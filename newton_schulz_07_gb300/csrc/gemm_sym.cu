@@ -4,14 +4,12 @@
 
 namespace mns {
 
-cudaError_t launch_sym_kk(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmArgs& args,
-                          int grid, cudaStream_t stream) {
-  return launch_tc_gemm<false, false, true, 8>(a, b, o, args, grid, stream);
+cudaError_t launch_sym_kk(const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_tc_gemm<false, false, true, 8>(p, grid, stream);
 }
 
-cudaError_t launch_sym_mnmn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmArgs& args,
-                            int grid, cudaStream_t stream) {
-  return launch_tc_gemm<true, true, true, 8>(a, b, o, args, grid, stream);
+cudaError_t launch_sym_mnmn(const GemmParams& p, int grid, cudaStream_t stream) {
+  return launch_tc_gemm<true, true, true, 8>(p, grid, stream);
 }
 
 }  // namespace mns

@@ -6,7 +6,7 @@
 // accumulation in TMEM by tcgen05.mma (M = 128, N = 256, K = 16 per
 // instruction), fp32 epilogue, one rounding to bf16.
 //
-// With the optional fp32 diagonal (GemmArgs::diag_out / diag_in) the
+// With the optional fp32 diagonal (GroupArgs::diag_out / diag_in) the
 // polynomial product stores B = D + O as an fp32 vector D = diag(B) and a bf16
 // matrix O with zero diagonal, and the update computes (a + D) X + O X; near
 // convergence B is close to a multiple of the identity, so this keeps the
@@ -98,15 +98,19 @@ __device__ __forceinline__ uint32_t stage_off(int row, int col) {
   return static_cast<uint32_t>(row * 64 + g * 16 + (col & 7) * 2);
 }
 
-struct GemmArgs {
+// A launch covers up to kMaxGroups stacks ("groups") of same-shape matrices,
+// each with its own tensor maps and sizes; the tile spaces of the groups are
+// concatenated, so one persistent launch keeps every SM busy across stacks.
+constexpr int kMaxGroups = 8;
+
+struct GroupArgs {
+  long long tile_begin;  // first tile of this group in the launch's tile space
   TileSpace space;
-  int M, N, K;        // output rows, output columns, contraction length
-  int num_kb;         // ceil(K / kBlockK)
-  uint16_t* out;      // bf16 [batch][M][N], row stride ld (written through the output tensor map)
-  const uint16_t* addend;  // same layout, or nullptr
+  int M, N, K;           // output rows, output columns, contraction length
+  int num_kb;            // ceil(K / kBlockK)
+  const uint16_t* addend;  // bf16 [batch][M][N] with row stride ld, or nullptr
   long long ld;
   long long bstride;
-  float alpha, beta;
   // Diagonal kept in fp32 (both optional):
   //   diag_out  SYM only: the fp32 value of each diagonal element is written to
   //             diag_out[b * M + i] and 0 is stored on the bf16 diagonal;
@@ -114,17 +118,33 @@ struct GemmArgs {
   //             the output row (diag_per_col == 0) or column (== 1).
   float* diag_out;
   const float* diag_in;
-  int diag_per_col;
   // Unscaled operands (optional): with norms != nullptr the operands are the
   // raw G of each matrix and s = 1 / (norms[b] + eps) is applied in the
   // epilogue, so the first step needs no scaled copy of G:
   //   SYM (Gram)      out = alpha s^2 acc
   //   FULL (update)   out = alpha s acc + (beta + diag) s addend
   const float* norms;
-  float eps;
+};
+
+struct GemmParams {
+  CUtensorMap tmA[kMaxGroups];    // A operand (rows of the output)
+  CUtensorMap tmB[kMaxGroups];    // B operand (columns of the output)
+  CUtensorMap tmOut[kMaxGroups];  // output, 32 x 32 boxes, 64-byte swizzle
+  GroupArgs grp[kMaxGroups];
+  int num_groups;
+  long long total_tiles;
+  float alpha, beta, eps;
+  int diag_per_col;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
+
+// Group owning global tile t (groups are few; a linear scan).
+__device__ __forceinline__ int find_group(const GemmParams& P, long long t) {
+  int g = 0;
+  while (g + 1 < P.num_groups && t >= P.grp[g + 1].tile_begin) ++g;
+  return g;
+}
 
 namespace detail {
 
@@ -182,8 +202,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
-    ns_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
+    ns_tc_gemm(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t tmem_base_sh;
@@ -214,9 +233,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ptx::mbar_init(sy.mma_done(), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-    ptx::prefetch_tensormap(&tmA);
-    ptx::prefetch_tensormap(&tmB);
-    ptx::prefetch_tensormap(&tmOut);
+    for (int g = 0; g < P.num_groups; ++g) {
+      ptx::prefetch_tensormap(&P.tmA[g]);
+      ptx::prefetch_tensormap(&P.tmB[g]);
+      ptx::prefetch_tensormap(&P.tmOut[g]);
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols);
@@ -233,8 +254,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();
 
-  const TileSpace& sp = args.space;
-  const int num_kb = args.num_kb;
+  const long long total = P.total_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -243,15 +263,20 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0;   // stages with a load issued at least once
       uint32_t issued_phase = 0;  // parity of the last load issued per stage
-      for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+      for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+        const int gr = find_group(P, t);
+        const GroupArgs& G = P.grp[gr];
+        const CUtensorMap* tmA = &P.tmA[gr];
+        const CUtensorMap* tmB = &P.tmB[gr];
+        const int num_kb = G.num_kb;
         int b, I, J;
-        tile_decode(sp, t, &b, &I, &J);
+        tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
         const int row0 = I * kTileM;
         const int col0 = J * kTileN;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.empty(stage), phase ^ 1u, abort_flag, args.err,
-                                    args.budget)) {
+          if (!detail::wait_bounded(sy.empty(stage), phase ^ 1u, abort_flag, P.err,
+                                    P.budget)) {
             ok = false;
             break;
           }
@@ -262,18 +287,18 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int c = 0; c < kTileM / kMnChunk; ++c)
-              ptx::tma_load_3d(sa + c * kMnChunkBytes, &tmA, sy.full(stage), row0 + c * kMnChunk,
+              ptx::tma_load_3d(sa + c * kMnChunkBytes, tmA, sy.full(stage), row0 + c * kMnChunk,
                                k0, b);
           } else {
-            ptx::tma_load_3d(sa, &tmA, sy.full(stage), k0, row0, b);
+            ptx::tma_load_3d(sa, tmA, sy.full(stage), k0, row0, b);
           }
           if (B_MN) {
 #pragma unroll
             for (int c = 0; c < kTileN / kMnChunk; ++c)
-              ptx::tma_load_3d(sb + c * kMnChunkBytes, &tmB, sy.full(stage), col0 + c * kMnChunk,
+              ptx::tma_load_3d(sb + c * kMnChunkBytes, tmB, sy.full(stage), col0 + c * kMnChunk,
                                k0, b);
           } else {
-            ptx::tma_load_3d(sb, &tmB, sy.full(stage), k0, col0, b);
+            ptx::tma_load_3d(sb, tmB, sy.full(stage), k0, col0, b);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -287,7 +312,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       // Wait for every copy still in flight before the CTA can exit.
 #pragma unroll
       for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, args.budget);
+        if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, P.budget);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -298,23 +323,26 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       uint32_t phase = 0;
       int buf = 0;
       uint32_t tphase = 0;
-      for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+      for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+        const int gr = find_group(P, t);
+        const GroupArgs& G = P.grp[gr];
+        const int num_kb = G.num_kb;
         // In a symmetric product, a tile on an even row tile I = 2J lies on the
         // diagonal 256-column block with its right half entirely above the
         // diagonal: only its left 128 columns are computed (N = 128).
         uint32_t idesc = idesc_full;
         if (SYM) {
           int b, I, J;
-          tile_decode(sp, t, &b, &I, &J);
+          tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
           if ((I & 1) == 0 && J == (I >> 1)) idesc = idesc_half;
         }
-        if (!detail::wait_bounded(sy.tempty(buf), tphase ^ 1u, abort_flag, args.err, args.budget))
+        if (!detail::wait_bounded(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.full(stage), phase, abort_flag, args.err, args.budget)) {
+          if (!detail::wait_bounded(sy.full(stage), phase, abort_flag, P.err, P.budget)) {
             ok = false;
             break;
           }
@@ -342,7 +370,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       }
       // Every MMA issued by this thread has finished once this arrives.
       ptx::mma_commit(sy.mma_done());
-      detail::drain_wait(sy.mma_done(), 0, args.budget);
+      detail::drain_wait(sy.mma_done(), 0, P.budget);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -357,12 +385,15 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const uint32_t stg = smem_base + kPipeBytes + static_cast<uint32_t>(e * kBufs * kChunkBytes);
     int buf = 0;
     uint32_t tphase = 0;
-    for (long long t = blockIdx.x; t < sp.total; t += gridDim.x) {
+    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+      const int gr = find_group(P, t);
+      const GroupArgs& G = P.grp[gr];
+      const CUtensorMap* tmOut = &P.tmOut[gr];
       int b, I, J;
-      tile_decode(sp, t, &b, &I, &J);
+      tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
       int ready = 0;
       if (lane == 0)
-        ready = detail::wait_bounded(sy.tfull(buf), tphase, abort_flag, args.err, args.budget) ? 1 : 0;
+        ready = detail::wait_bounded(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       __syncwarp();
@@ -370,28 +401,28 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 
       const long long gi = static_cast<long long>(I) * kTileM + r_in_tile;
       const int warp_row_max = I * kTileM + q * 32 + 31;
-      const bool row_ok = gi < args.M;
+      const bool row_ok = gi < G.M;
       const uint16_t* addm =
-          args.addend ? args.addend + static_cast<long long>(b) * args.bstride : nullptr;
+          G.addend ? G.addend + static_cast<long long>(b) * G.bstride : nullptr;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * kTileN);
       const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
       // Addend coefficient: per row (row-indexed diagonal or none) ...
       float mscale = 1.0f;  // per-matrix scale of unscaled operands
-      if (args.norms != nullptr) mscale = 1.0f / (__ldg(args.norms + b) + args.eps);
-      const float alpha_t = SYM ? args.alpha * (mscale * mscale) : args.alpha * mscale;
-      float row_coef = args.beta;
-      if (!SYM && args.diag_in != nullptr && !args.diag_per_col && row_ok)
-        row_coef += __ldg(args.diag_in + static_cast<long long>(b) * args.M + gi);
+      if (G.norms != nullptr) mscale = 1.0f / (__ldg(G.norms + b) + P.eps);
+      const float alpha_t = SYM ? P.alpha * (mscale * mscale) : P.alpha * mscale;
+      float row_coef = P.beta;
+      if (!SYM && G.diag_in != nullptr && !P.diag_per_col && row_ok)
+        row_coef += __ldg(G.diag_in + static_cast<long long>(b) * G.M + gi);
       row_coef *= mscale;
       // ... or per column, staged in shared memory for this warp's columns.
-      const bool col_mode = !SYM && args.diag_in != nullptr && args.diag_per_col;
+      const bool col_mode = !SYM && G.diag_in != nullptr && P.diag_per_col;
       if (col_mode) {
 #pragma unroll
         for (int v = 0; v < kChunksPerWarp; ++v) {
           const int col = col_base + v * 32 + lane;
           colc[v * 32 + lane] =
-              (args.beta + (col < args.N ? __ldg(args.diag_in + static_cast<long long>(b) * args.N + col) : 0.0f)) *
+              (P.beta + (col < G.N ? __ldg(G.diag_in + static_cast<long long>(b) * G.N + col) : 0.0f)) *
               mscale;
         }
         __syncwarp();
@@ -402,11 +433,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int gj0 = col_base + cc * 32;
 #pragma unroll
         for (int g = 0; g < 4; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
-        if (addm == nullptr || !row_ok || gj0 >= args.N || (SYM && gj0 > gi)) return;
-        const uint4* src = reinterpret_cast<const uint4*>(addm + gi * args.ld + gj0);
+        if (addm == nullptr || !row_ok || gj0 >= G.N || (SYM && gj0 > gi)) return;
+        const uint4* src = reinterpret_cast<const uint4*>(addm + gi * G.ld + gj0);
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          if (gj0 + 8 * g + 8 <= args.N) dst[g] = __ldg(src + g);
+          if (gj0 + 8 * g + 8 <= G.N) dst[g] = __ldg(src + g);
       };
       uint4 av[4];
       load_addend(0, av);
@@ -414,7 +445,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 #pragma unroll 1
       for (int cc = 0; cc < kChunksPerWarp; ++cc) {
         const int gj0 = col_base + cc * 32;
-        if (gj0 >= args.N) break;                   // warp-uniform
+        if (gj0 >= G.N) break;                   // warp-uniform
         if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
         uint4 an[4];
         if (cc + 1 < kChunksPerWarp) load_addend(cc + 1, an);
@@ -447,7 +478,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             }
           }
         }
-        if (SYM && args.diag_out != nullptr && row_ok && gi >= gj0 && gi < gj0 + 32) {
+        if (SYM && G.diag_out != nullptr && row_ok && gi >= gj0 && gi < gj0 + 32) {
           // The diagonal element goes to the fp32 side vector; 0 is stored.
           float dval = 0.0f;
 #pragma unroll
@@ -457,7 +488,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               f[j] = 0.0f;
             }
           }
-          args.diag_out[static_cast<long long>(b) * args.M + gi] = dval;
+          G.diag_out[static_cast<long long>(b) * G.M + gi] = dval;
         }
         uint32_t hv[16];
 #pragma unroll
@@ -479,7 +510,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
+            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::bulk_commit();
           }
         } else if (gj0 < R0) {
@@ -497,8 +528,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
-            ptx::tma_store_3d(&tmOut, tr, R0, gj0, b);
+            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
+            ptx::tma_store_3d(tmOut, tr, R0, gj0, b);
             ptx::bulk_commit();
           }
         } else {
@@ -514,7 +545,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmOut, d, gj0, R0, b);
+            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::bulk_commit();
           }
         }

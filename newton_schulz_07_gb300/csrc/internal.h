@@ -9,22 +9,14 @@
 
 namespace mns {
 
-struct GemmArgs;
+struct GemmParams;
 
-// Tensor maps: a, b = operands; o = output (32 x 32 boxes, 64-byte swizzle).
 // Gram / polynomial products: lower-triangle tiles, mirrored stores.
-cudaError_t launch_sym_kk(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                          const GemmArgs& args,
-                          int grid, cudaStream_t stream);  // both operands K-major
-cudaError_t launch_sym_mnmn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                          const GemmArgs& args,
-                            int grid, cudaStream_t stream);  // both operands MN-major
-// Update products: full output grid.
-cudaError_t launch_full_kmn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                          const GemmArgs& args,
-                            int grid, cudaStream_t stream);  // B operand MN-major
-cudaError_t launch_full_kk(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                          const GemmArgs& args,
-                           int grid, cudaStream_t stream);  // both operands K-major
+cudaError_t launch_sym_kk(const GemmParams& p, int grid, cudaStream_t stream);    // K-major operands
+cudaError_t launch_sym_mnmn(const GemmParams& p, int grid, cudaStream_t stream);  // MN-major operands
+// Update products: full output grid.  `max_k` is the largest contraction of
+// the launch's groups (short contractions use 8 epilogue warps).
+cudaError_t launch_full_kmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
 
 }  // namespace mns

@@ -27,7 +27,6 @@
 
 namespace {
 
-using mns::GemmArgs;
 
 constexpr long long kMaxDim = 1 << 20;
 constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
@@ -167,105 +166,134 @@ bool make_map(CUtensorMap* map, const void* base, long long inner, long long row
 
 // ---------------------------------------------------------------- launches --
 
-GemmArgs base_args(int sym, long long batch, long long M, long long N, long long K, int* err) {
-  GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
-                                 static_cast<int>(N));
-  a.M = static_cast<int>(M);
-  a.N = static_cast<int>(N);
-  a.K = static_cast<int>(K);
-  a.num_kb = static_cast<int>((K + mns::kBlockK - 1) / mns::kBlockK);
-  a.ld = N;
-  a.bstride = M * N;
-  a.alpha = 1.0f;
-  a.beta = 0.0f;
-  a.err = err;
-  a.budget = kWaitBudgetCycles;
-  return a;
-}
-
 // Output map: [batch][M][N] bf16, 32 x 32 boxes, 64-byte swizzle.
 bool make_out_map(CUtensorMap* map, const void* base, long long M, long long N, long long batch) {
   return make_map(map, base, N, M, batch, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int grid_for(const GemmArgs& a, int sms) {
-  const long long g = a.space.total < sms ? a.space.total : sms;
+int grid_for(long long tiles, int sms) {
+  const long long g = tiles < sms ? tiles : sms;
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? MUON_NS_OK : MUON_NS_ERR_CUDA; }
 
-int run_gram(const Problem& p, const uint16_t* X, uint16_t* A, const float* norms, float eps,
-             int* err, int sms, cudaStream_t st) {
-  CUtensorMap ta, tb, to;
-  GemmArgs a = base_args(1, p.batch, p.m, p.m, p.n, err);
-  a.out = A;
-  a.norms = norms;
-  a.eps = eps;
-  if (!make_out_map(&to, A, p.m, p.m, p.batch)) return MUON_NS_ERR_CUDA;
-  if (!p.T) {
-    // X [batch][m][n]: rows of X are the K-major operand rows.
-    if (!make_map(&ta, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
-        !make_map(&tb, X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileN))
-      return MUON_NS_ERR_CUDA;
-    return to_status(mns::launch_sym_kk(ta, tb, to, a, grid_for(a, sms), st));
+// One stack's buffers for one NS step.  All stacks of one launch share the
+// orientation (p.T), because operand majorness is a kernel template argument.
+struct StepIO {
+  Problem p;
+  const uint16_t* X;   // the iterate, or the raw G in the first step
+  uint16_t* A;         // Gram output / polynomial input
+  uint16_t* B;         // polynomial output (zero diagonal) / update input
+  float* D;            // fp32 diagonal of B
+  const float* norms;  // non-null in the first step: X is unscaled
+  uint16_t* Xn;        // update output
+};
+
+// Launch parameters (about 4 KB) are built on the host and copied at launch.
+mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err) {
+  static thread_local mns::GemmParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.num_groups = ng;
+  P.alpha = alpha;
+  P.beta = beta;
+  P.eps = eps;
+  P.err = err;
+  P.budget = kWaitBudgetCycles;
+  return &P;
+}
+
+void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M, long long N,
+               long long K, long long* total) {
+  mns::GroupArgs& G = P->grp[i];
+  G.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
+                                 static_cast<int>(N));
+  G.tile_begin = *total;
+  *total += G.space.total;
+  G.M = static_cast<int>(M);
+  G.N = static_cast<int>(N);
+  G.K = static_cast<int>(K);
+  G.num_kb = static_cast<int>((K + mns::kBlockK - 1) / mns::kBlockK);
+  G.ld = N;
+  G.bstride = M * N;
+}
+
+int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_t st) {
+  mns::GemmParams* P = new_params(ng, 1.0f, 0.0f, eps, err);
+  long long total = 0;
+  const bool T = io[0].p.T;
+  for (int i = 0; i < ng; ++i) {
+    const Problem& p = io[i].p;
+    set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total);
+    P->grp[i].norms = io[i].norms;
+    if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch)) return MUON_NS_ERR_CUDA;
+    if (!T) {
+      // X [batch][m][n]: rows of X are the K-major operand rows.
+      if (!make_map(&P->tmA[i], io[i].X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileN))
+        return MUON_NS_ERR_CUDA;
+    } else {
+      // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
+      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, mns::kMnChunk, mns::kBlockK))
+        return MUON_NS_ERR_CUDA;
+      P->tmB[i] = P->tmA[i];
+    }
   }
-  // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
-  if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kMnChunk, mns::kBlockK)) return MUON_NS_ERR_CUDA;
-  return to_status(mns::launch_sym_mnmn(ta, ta, to, a, grid_for(a, sms), st));
+  P->total_tiles = total;
+  const int grid = grid_for(total, sms);
+  return to_status(T ? mns::launch_sym_mnmn(*P, grid, st) : mns::launch_sym_kk(*P, grid, st));
 }
 
-int run_poly(long long batch, long long m, const uint16_t* A, uint16_t* B, float* diag, float b,
-             float c, int* err, int sms, cudaStream_t st) {
-  CUtensorMap ta, tb, to;
-  if (!make_map(&ta, A, m, m, batch, mns::kBlockK, mns::kTileM) ||
-      !make_map(&tb, A, m, m, batch, mns::kBlockK, mns::kTileN) ||
-      !make_out_map(&to, B, m, m, batch))
-    return MUON_NS_ERR_CUDA;
-  GemmArgs a = base_args(1, batch, m, m, m, err);
-  a.out = B;
-  a.addend = A;
-  a.alpha = c;
-  a.beta = b;
-  a.diag_out = diag;
-  return to_status(mns::launch_sym_kk(ta, tb, to, a, grid_for(a, sms), st));
+int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cudaStream_t st) {
+  mns::GemmParams* P = new_params(ng, c, b, 0.0f, err);
+  long long total = 0;
+  for (int i = 0; i < ng; ++i) {
+    const long long m = io[i].p.m, batch = io[i].p.batch;
+    set_group(P, i, 1, batch, m, m, m, &total);
+    P->grp[i].addend = io[i].A;
+    P->grp[i].diag_out = io[i].D;
+    if (!make_map(&P->tmA[i], io[i].A, m, m, batch, mns::kBlockK, mns::kTileM) ||
+        !make_map(&P->tmB[i], io[i].A, m, m, batch, mns::kBlockK, mns::kTileN) ||
+        !make_out_map(&P->tmOut[i], io[i].B, m, m, batch))
+      return MUON_NS_ERR_CUDA;
+  }
+  P->total_tiles = total;
+  return to_status(mns::launch_sym_kk(*P, grid_for(total, sms), st));
 }
 
-int run_update(const Problem& p, const uint16_t* X, const uint16_t* B, const float* diag,
-               uint16_t* Xn, float alpha_x, const float* norms, float eps, int* err, int sms,
+int run_update(const StepIO* io, int ng, float alpha_x, float eps, int* err, int sms,
                cudaStream_t st) {
-  CUtensorMap ta, tb, to;
-  if (!make_out_map(&to, Xn, p.T ? p.n : p.m, p.T ? p.m : p.n, p.batch)) return MUON_NS_ERR_CUDA;
-  if (!p.T) {
-    // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
-    if (!make_map(&ta, B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
-        !make_map(&tb, X, p.n, p.m, p.batch, mns::kMnChunk, mns::kBlockK))
-      return MUON_NS_ERR_CUDA;
-    GemmArgs a = base_args(0, p.batch, p.m, p.n, p.m, err);
-    a.out = Xn;
-    a.addend = X;
-    a.beta = alpha_x;
-    a.diag_in = diag;  // (a + D_i) scales row i of X
-    a.diag_per_col = 0;
-    a.norms = norms;
-    a.eps = eps;
-    return to_status(mns::launch_full_kmn(ta, tb, to, a, grid_for(a, sms), st));
+  mns::GemmParams* P = new_params(ng, 1.0f, alpha_x, eps, err);
+  long long total = 0;
+  const bool T = io[0].p.T;
+  int max_k = 0;
+  P->diag_per_col = T ? 1 : 0;  // (a + D_i) scales row i of X, or column i of Y
+  for (int i = 0; i < ng; ++i) {
+    const Problem& p = io[i].p;
+    if (!T) {
+      // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
+      set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total);
+      if (!make_map(&P->tmA[i], io[i].B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mns::kMnChunk, mns::kBlockK) ||
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch))
+        return MUON_NS_ERR_CUDA;
+    } else {
+      // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
+      set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total);
+      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, mns::kBlockK, mns::kTileM) ||
+          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileN) ||
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch))
+        return MUON_NS_ERR_CUDA;
+    }
+    P->grp[i].addend = io[i].X;
+    P->grp[i].diag_in = io[i].D;
+    P->grp[i].norms = io[i].norms;
+    if (p.m > max_k) max_k = static_cast<int>(p.m);
   }
-  // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
-  if (!make_map(&ta, X, p.m, p.n, p.batch, mns::kBlockK, mns::kTileM) ||
-      !make_map(&tb, B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileN))
-    return MUON_NS_ERR_CUDA;
-  GemmArgs a = base_args(0, p.batch, p.n, p.m, p.m, err);
-  a.out = Xn;
-  a.addend = X;
-  a.beta = alpha_x;
-  a.diag_in = diag;  // Y D: (a + D_j) scales column j of Y
-  a.diag_per_col = 1;
-  a.norms = norms;
-  a.eps = eps;
-  return to_status(mns::launch_full_kk(ta, tb, to, a, grid_for(a, sms), st));
+  P->total_tiles = total;
+  const int grid = grid_for(total, sms);
+  return to_status(T ? mns::launch_full_kk(*P, max_k, grid, st)
+                     : mns::launch_full_kmn(*P, max_k, grid, st));
 }
 
 int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* X, float eps,
@@ -288,42 +316,90 @@ int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t
   return MUON_NS_OK;
 }
 
+// One stack of a (possibly grouped) NS call.
+struct Stack {
+  Problem p;
+  Layout L;
+  const uint16_t* G;
+  uint16_t* out;
+  uint8_t* ws;  // this stack's workspace (layout L)
+  uint16_t* cur;
+};
+
+// NS of several stacks, all kernels reporting to `err`.  Stacks are launched
+// together, per orientation, in launches of at most kMaxGroups groups.
+int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, int* err, int sms,
+                  cudaStream_t st) {
+  int s = MUON_NS_OK;
+  if (steps == 0) {
+    for (int i = 0; i < ns; ++i)
+      if ((s = run_normalize(S[i].p, S[i].L, S[i].G, S[i].out, eps, S[i].ws, st)) != MUON_NS_OK)
+        return s;
+    return MUON_NS_OK;
+  }
+  // Norms only; the first step reads G itself and applies s = 1/(norm + eps)
+  // in its epilogues (A0 = s^2 G G^T, X1 = s O G + s (a + D) G), so no scaled
+  // copy of G is written or read.
+  for (int i = 0; i < ns; ++i)
+    if ((s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st)) != MUON_NS_OK)
+      return s;
+  StepIO io[mns::kMaxGroups];
+  int members[mns::kMaxGroups];
+  for (int k = 0; k < steps; ++k) {
+    for (int cls = 0; cls < 2; ++cls) {  // wide stacks, then tall stacks
+      int i = 0;
+      while (i < ns) {
+        int ng = 0;
+        for (; i < ns && ng < mns::kMaxGroups; ++i) {
+          if (static_cast<int>(S[i].p.T) != cls) continue;
+          Stack& t = S[i];
+          uint16_t* wsx = reinterpret_cast<uint16_t*>(t.ws + t.L.x);
+          // Iterates alternate between the workspace and `out` so that the
+          // last lands in `out`; in place (out == G) the first iterate must
+          // not overwrite G while step 1 still reads it.
+          uint16_t* nxt;
+          if (k == 0)
+            nxt = (t.out == t.G || steps % 2 == 0) ? wsx : t.out;
+          else
+            nxt = (t.cur == t.out) ? wsx : t.out;
+          StepIO& e = io[ng];
+          e.p = t.p;
+          e.X = (k == 0) ? t.G : t.cur;
+          e.A = reinterpret_cast<uint16_t*>(t.ws + t.L.a);
+          e.B = reinterpret_cast<uint16_t*>(t.ws + t.L.b);
+          e.D = reinterpret_cast<float*>(t.ws + t.L.diag);
+          e.norms = (k == 0) ? reinterpret_cast<const float*>(t.ws + t.L.norms) : nullptr;
+          e.Xn = nxt;
+          members[ng++] = i;
+        }
+        if (ng == 0) continue;
+        if ((s = run_gram(io, ng, eps, err, sms, st)) != MUON_NS_OK) return s;
+        if ((s = run_poly(io, ng, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
+        if ((s = run_update(io, ng, abc[0], eps, err, sms, st)) != MUON_NS_OK) return s;
+        for (int j = 0; j < ng; ++j) S[members[j]].cur = io[j].Xn;
+      }
+    }
+  }
+  for (int i = 0; i < ns; ++i)
+    if (S[i].cur != S[i].out &&
+        cudaMemcpyAsync(S[i].out, S[i].cur, S[i].L.x_bytes, cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+      return MUON_NS_ERR_CUDA;
+  return MUON_NS_OK;
+}
+
 int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, int steps,
            const float abc[3], float eps, uint8_t* ws, int sms, cudaStream_t st) {
   int* err = reinterpret_cast<int*>(ws + L.error);
   if (cudaMemsetAsync(ws + L.error, 0, 256, st) != cudaSuccess) return MUON_NS_ERR_CUDA;
-  uint16_t* wsx = reinterpret_cast<uint16_t*>(ws + L.x);
-  uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
-  uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
-  float* D = reinterpret_cast<float*>(ws + L.diag);
-  const float* norms = reinterpret_cast<const float*>(ws + L.norms);
-  if (steps == 0) return run_normalize(p, L, G, out, eps, ws, st);
-  // Norms only; the first step reads G itself and applies s = 1/(norm + eps)
-  // in its epilogues (A0 = s^2 G G^T, X1 = s O G + s (a + D) G), so no scaled
-  // copy of G is written or read.
-  int s = run_normalize(p, L, G, nullptr, eps, ws, st);
-  if (s != MUON_NS_OK) return s;
-  // Iterates alternate between the workspace and `out` so that the last one
-  // lands in `out`; in place (out == G) the first iterate must not overwrite
-  // G while step 1 still reads it, so it goes to the workspace and an odd step
-  // count ends with one copy.
-  const bool in_place = out == G;
-  uint16_t* cur = (in_place || steps % 2 == 0) ? wsx : out;
-  if ((s = run_gram(p, G, A, norms, eps, err, sms, st)) != MUON_NS_OK) return s;
-  if ((s = run_poly(p.batch, p.m, A, B, D, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-  if ((s = run_update(p, G, B, D, cur, abc[0], norms, eps, err, sms, st)) != MUON_NS_OK) return s;
-  for (int k = 1; k < steps; ++k) {
-    uint16_t* nxt = (cur == out) ? wsx : out;
-    if ((s = run_gram(p, cur, A, nullptr, 0.0f, err, sms, st)) != MUON_NS_OK) return s;
-    if ((s = run_poly(p.batch, p.m, A, B, D, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-    if ((s = run_update(p, cur, B, D, nxt, abc[0], nullptr, 0.0f, err, sms, st)) != MUON_NS_OK)
-      return s;
-    cur = nxt;
-  }
-  if (cur != out &&
-      cudaMemcpyAsync(out, cur, L.x_bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return MUON_NS_ERR_CUDA;
-  return MUON_NS_OK;
+  Stack S;
+  S.p = p;
+  S.L = L;
+  S.G = G;
+  S.out = out;
+  S.ws = ws;
+  S.cur = nullptr;
+  return run_ns_stacks(&S, 1, steps, abc, eps, err, sms, st);
 }
 
 int check_scalars(int steps, const float* coeffs, float eps, float abc[3]) {
@@ -539,7 +615,12 @@ int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols
   if (!aligned16(X) || !aligned16(A)) return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_gram(p, X, A, norms, eps, device_error, d.sms, stream);
+  StepIO io = {};
+  io.p = p;
+  io.X = X;
+  io.A = A;
+  io.norms = norms;
+  return run_gram(&io, 1, eps, device_error, d.sms, stream);
 }
 
 int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
@@ -554,7 +635,12 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m
   if (!aligned16(A) || !aligned16(B) || !aligned16(diag)) return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_poly(p.batch, p.m, A, B, diag, b, c, device_error, d.sms, stream);
+  StepIO io = {};
+  io.p = p;
+  io.A = const_cast<uint16_t*>(A);
+  io.B = B;
+  io.D = diag;
+  return run_poly(&io, 1, b, c, device_error, d.sms, stream);
 }
 
 int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
@@ -572,7 +658,14 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, mu
     return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_update(p, X, B, diag, Xn, a, norms, eps, device_error, d.sms, stream);
+  StepIO io = {};
+  io.p = p;
+  io.X = X;
+  io.B = const_cast<uint16_t*>(B);
+  io.D = const_cast<float*>(diag);
+  io.norms = norms;
+  io.Xn = Xn;
+  return run_update(&io, 1, a, eps, device_error, d.sms, stream);
 }
 
 int muon_ns_launches_per_call(int steps) {
