@@ -140,6 +140,39 @@ int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols
 int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
             const float* coeffs, float eps, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Several stacks in one call (e.g. every Muon parameter group of an optimizer
+ * step): same-shape matrices are stacked, as param-decomp PR #978 (What)
+ * stacks same-shape leaves; stacks of different shapes run through the same
+ * launches, so small stacks do not leave SMs idle.
+ * ------------------------------------------------------------------------- */
+
+/* One stack of a grouped call: `batch` matrices of rows x cols, device bf16,
+ * contiguous [batch][rows][cols]; out == G allowed, otherwise no overlap
+ * (with any other stack either). */
+typedef struct {
+  const muon_bf16* G;
+  muon_bf16* out;
+  int batch;
+  int rows;
+  int cols;
+} muon_ns_stack;
+
+/* Workspace bytes for muon_ns_grouped(): the per-stack workspaces of
+ * muon_ns_workspace_size() laid end to end (non-empty stacks, in order). */
+int muon_ns_grouped_workspace_size(const muon_ns_stack* stacks, int num_stacks, size_t* bytes);
+
+/* NS of every stack (host array of num_stacks <= 64 descriptors) with one set
+ * of steps / coefficients / eps.  Each step runs as one Gram, one polynomial
+ * and one update launch for up to 8 stacks of the same orientation (wide:
+ * rows <= cols; tall: rows > cols) at a time, plus one norm launch per stack.
+ * Results are bit-identical to calling muon_ns_ws() on each stack alone.
+ * The device error word is the first 4 bytes of the workspace
+ * (muon_ns_read_error).  Validation, aliasing and errors as for muon_ns_ws;
+ * empty stacks are skipped. */
+int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, const float* coeffs,
+                    float eps, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, copies the device error word of `workspace` into
  * *device_error (0 = none) and, if `clear` is nonzero, resets it.  Returns
  * MUON_NS_ERR_TIMEOUT if the word is nonzero, else MUON_NS_OK or an error. */

@@ -11,6 +11,8 @@ from .ns import (  # noqa: F401
     launches_per_call,
     muon_ns,
     muon_ns_gram,
+    muon_ns_grouped,
+    grouped_workspace_size,
     muon_ns_normalize,
     muon_ns_normalize_static,
     muon_ns_poly,

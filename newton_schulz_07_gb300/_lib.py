@@ -26,6 +26,14 @@ _pf = ctypes.POINTER(ctypes.c_float)
 _pi = ctypes.POINTER(ctypes.c_int)
 _psz = ctypes.POINTER(ctypes.c_size_t)
 
+class MuonNSStack(ctypes.Structure):
+    """muon_ns_stack of include/muon_ns.h."""
+    _fields_ = [("G", ctypes.c_void_p), ("out", ctypes.c_void_p), ("batch", ctypes.c_int),
+                ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
+
+
+_pst = ctypes.POINTER(MuonNSStack)
+
 # name -> (restype, argtypes); the exported C ABI, in header order.
 SIGNATURES = {
     "muon_ns_version": (ctypes.c_char_p, []),
@@ -35,6 +43,8 @@ SIGNATURES = {
     "muon_ns_workspace_region": (_c_int, [_c_int, _c_int, _c_int, _c_int, _psz, _psz]),
     "muon_ns_ws": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp]),
+    "muon_ns_grouped_workspace_size": (_c_int, [_pst, _c_int, _psz]),
+    "muon_ns_grouped": (_c_int, [_pst, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),
     "muon_ns_cached_error": (_c_int, [_c_int, _pi]),
     "muon_ns_normalize": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp]),

@@ -545,6 +545,61 @@ int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, i
   return run_ns(p, L, G, out, steps, abc, eps, static_cast<uint8_t*>(c.ptr), d.sms, stream);
 }
 
+int muon_ns_grouped_workspace_size(const muon_ns_stack* stacks, int num_stacks, size_t* bytes) {
+  if (!bytes || num_stacks < 0 || num_stacks > 64 || (num_stacks > 0 && !stacks))
+    return MUON_NS_ERR_INVALID_ARG;
+  size_t total = 0;
+  for (int i = 0; i < num_stacks; ++i) {
+    Problem p;
+    bool empty;
+    const int s = check_shape(stacks[i].batch, stacks[i].rows, stacks[i].cols, &p, &empty);
+    if (s != MUON_NS_OK) return s;
+    if (!empty) total += make_layout(p).total;
+  }
+  *bytes = total;
+  return MUON_NS_OK;
+}
+
+int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, const float* coeffs,
+                    float eps, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (num_stacks < 0 || num_stacks > 64 || (num_stacks > 0 && !stacks)) return MUON_NS_ERR_INVALID_ARG;
+  float abc[3];
+  int s = check_scalars(steps, coeffs, eps, abc);
+  if (s != MUON_NS_OK) return s;
+  Stack S[64];
+  size_t offsets[64];
+  int ns = 0;
+  size_t off = 0;
+  for (int i = 0; i < num_stacks; ++i) {
+    Problem p;
+    bool empty;
+    if ((s = check_shape(stacks[i].batch, stacks[i].rows, stacks[i].cols, &p, &empty)) != MUON_NS_OK)
+      return s;
+    if (empty) continue;
+    if (!stacks[i].G || !stacks[i].out) return MUON_NS_ERR_INVALID_ARG;
+    if (!aligned16(stacks[i].G) || !aligned16(stacks[i].out)) return MUON_NS_ERR_ALIGNMENT;
+    Stack& t = S[ns];
+    t.p = p;
+    t.L = make_layout(p);
+    t.G = stacks[i].G;
+    t.out = stacks[i].out;
+    t.ws = nullptr;
+    t.cur = nullptr;
+    offsets[ns++] = off;
+    off += t.L.total;
+  }
+  if (ns == 0) return MUON_NS_OK;
+  if (!workspace || workspace_bytes < off) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  for (int i = 0; i < ns; ++i) S[i].ws = base + offsets[i];
+  int* err = reinterpret_cast<int*>(base + S[0].L.error);
+  if (cudaMemsetAsync(base, 0, 256, stream) != cudaSuccess) return MUON_NS_ERR_CUDA;
+  return run_ns_stacks(S, ns, steps, abc, eps, err, d.sms, stream);
+}
+
 int muon_ns_read_error(const void* workspace, int* device_error, int clear, cudaStream_t stream) {
   if (!workspace || !device_error) return MUON_NS_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) {

@@ -181,3 +181,46 @@ def muon_ns_normalize_static(G: torch.Tensor, eps: float = DEFAULT_EPS, X: torch
         _lib.check(_lib.lib().muon_ns_normalize_static(_ptr(G), _ptr(X), b, r, c, float(eps), _stream(G.device)),
                    "muon_ns_normalize_static")
     return X
+
+
+def _stack_array(Gs, outs):
+    arr = (_lib.MuonNSStack * max(len(Gs), 1))()
+    for i, (G, o) in enumerate(zip(Gs, outs)):
+        b, r, c = _shape3(G)
+        arr[i] = _lib.MuonNSStack(G.data_ptr(), o.data_ptr(), b, r, c)
+    return arr
+
+
+def grouped_workspace_size(Gs) -> int:
+    arr = _stack_array(Gs, Gs)
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_grouped_workspace_size(arr, len(Gs), ctypes.byref(n)),
+               "muon_ns_grouped_workspace_size")
+    return n.value
+
+
+def muon_ns_grouped(Gs, outs=None, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS,
+                    workspace: torch.Tensor | None = None):
+    """NS of several stacks (a list of bf16 CUDA matrices or stacks, any shapes)
+    in one call; returns the list of outputs (`outs[i]` may be `Gs[i]`)."""
+    Gs = list(Gs)
+    if not Gs:
+        return []
+    dev = Gs[0].device
+    for G in Gs:
+        _check_bf16(G, "G")
+        if G.device != dev:
+            raise ValueError("all stacks must be on one device")
+    outs = [torch.empty_like(G) for G in Gs] if outs is None else list(outs)
+    for G, o in zip(Gs, outs):
+        _check_bf16(o, "out")
+        if o.shape != G.shape or o.device != dev:
+            raise ValueError("outs must match Gs")
+    if workspace is None:
+        workspace = torch.empty(max(grouped_workspace_size(Gs), 1), dtype=torch.uint8, device=dev)
+    arr = _stack_array(Gs, outs)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.lib().muon_ns_grouped(arr, len(Gs), int(steps), _coeffs(coeffs), float(eps),
+                                              _ptr(workspace), workspace.numel(), _stream(dev)),
+                   "muon_ns_grouped")
+    return outs

@@ -246,3 +246,23 @@ def _chunk_store_writes(m, ts, warps_per_quarter=2):
 @pytest.mark.parametrize("m", [8, 136, 256, 392, 640, 1000, 1536])
 def test_symmetric_bulk_stores_write_each_block_once(m):
     assert np.all(_chunk_store_writes(m, tiles(0, 1, m, m)) == 1)
+
+
+def test_grouped_workspace_is_sum_of_stack_workspaces():
+    shapes = [(3, 136, 264), (2, 264, 136), (0, 8, 8), (1, 392, 392)]
+    arr = (_lib.MuonNSStack * len(shapes))()
+    for i, (b, r, c) in enumerate(shapes):
+        arr[i] = _lib.MuonNSStack(4096, 4096, b, r, c)
+    n = ctypes.c_size_t(0)
+    L = _lib.lib()
+    assert L.muon_ns_grouped_workspace_size(arr, len(shapes), ctypes.byref(n)) == _lib.OK
+    assert n.value == sum(_ws(b, r, c)[1] for b, r, c in shapes)
+    arr[1] = _lib.MuonNSStack(4096, 4096, 2, 264, 130)
+    assert L.muon_ns_grouped_workspace_size(arr, len(shapes), ctypes.byref(n)) == _lib.ERR_ALIGNMENT
+    assert L.muon_ns_grouped(arr, 65, 5, None, 1e-7, ctypes.c_void_p(4096), 1 << 30, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_grouped(None, 0, 5, None, 1e-7, None, 0, None) == _lib.OK
+    arr[1] = _lib.MuonNSStack(4096, 0, 2, 264, 136)
+    assert L.muon_ns_grouped(arr, len(shapes), 5, None, 1e-7, ctypes.c_void_p(4096), 1 << 30,
+                             None) == _lib.ERR_INVALID_ARG
+    arr[1] = _lib.MuonNSStack(4096, 4096, 2, 264, 136)
+    assert L.muon_ns_grouped(arr, len(shapes), 5, None, 1e-7, ctypes.c_void_p(4096), 16, None) == _lib.ERR_WORKSPACE
