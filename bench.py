@@ -406,6 +406,8 @@ def main():
             if name == w.name:
                 continue
             per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
+        mixed = [ns_inputs.WORKLOADS["stack_32x7168x2048"], ns_inputs.WORKLOADS["stack_128x2048x768"]]
+        per_shape["mixed_stacks_32x7168x2048+128x2048x768"] = time_grouped(torch, ns, mixed, dev, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -479,6 +481,40 @@ def time_workload(torch, ns, w, dev, peaks, steps=10, warmup=3):
     if w.name in PAGES_H200_QUACK_MS:
         res["pages_h200_quack_ms"] = PAGES_H200_QUACK_MS[w.name]
     del G, out, ws, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_grouped(torch, ns, wls, dev, peaks, steps=10, warmup=3):
+    """One muon_ns_grouped call over several stacks (one optimizer step's NS
+    over parameter groups of different shapes)."""
+    Gs = [torch.from_numpy(ns_inputs.stack_bits(w).view(np.int16)).view(torch.bfloat16).to(dev) for w in wls]
+    outs = [torch.empty_like(G) for G in Gs]
+    ws = torch.empty(ns.grouped_workspace_size(Gs), dtype=torch.uint8, device=dev)
+    scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        ns.muon_ns_grouped(Gs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    tot = 0.0
+    for i in range(steps):
+        scrub.fill_(i & 0xFF)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        ns.muon_ns_grouped(Gs, outs=outs, workspace=ws)
+        e.record(stream)
+        torch.cuda.synchronize()
+        tot += s.elapsed_time(e)
+    ms = tot / steps
+    dense = sum(w.dense_flops() for w in wls)
+    tf = dense / (ms * 1e-3) / 1e12
+    res = {"ms": ms, "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
+           "stacks": [w.name for w in wls], "api": "muon_ns_grouped (one call)", "steps": steps,
+           "l2": "flushed between timed steps", "device_error_word": ns.read_error(ws)}
+    if all(w.name in PAGES_H200_QUACK_MS for w in wls):
+        res["pages_h200_quack_ms_sum"] = sum(PAGES_H200_QUACK_MS[w.name] for w in wls)
+    del Gs, outs, ws, scrub
     torch.cuda.empty_cache()
     return res
 
