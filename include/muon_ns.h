@@ -141,6 +141,29 @@ int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, i
             const float* coeffs, float eps, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * fp32 NS (the `ns_dtype: float32` setting of param-decomp PR #978, What).
+ * G and out are fp32 [batch][rows][cols]; X, A and B are stored in fp32
+ * rounded to tf32 (10-bit mantissa, round to nearest even) and multiplied on
+ * the tf32 tensor cores with fp32 accumulation; the epilogues, B's diagonal
+ * and the final output are full fp32.  About 7x closer to the exact result
+ * than the bf16 path, at about twice its time and memory.  Same argument
+ * rules as the bf16 calls (rows and cols multiples of 8, 16-byte aligned
+ * pointers, out == G allowed).
+ * ------------------------------------------------------------------------- */
+
+/* Workspace bytes / regions for muon_ns_ws_f32 (regions as for the bf16 call,
+ * with fp32 X, GRAM and POLY regions). */
+int muon_ns_f32_workspace_size(int batch, int rows, int cols, size_t* bytes);
+int muon_ns_f32_workspace_region(int batch, int rows, int cols, int region, size_t* offset,
+                                 size_t* bytes);
+
+/* out = NS(G) in fp32 mode; otherwise as muon_ns_ws().  Launches per call:
+ * 1 + 3 * steps (2 if steps == 0). */
+int muon_ns_ws_f32(const float* G, float* out, int batch, int rows, int cols, int steps,
+                   const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Several stacks in one call (e.g. every Muon parameter group of an optimizer
  * step): same-shape matrices are stacked, as param-decomp PR #978 (What)
  * stacks same-shape leaves; stacks of different shapes run through the same

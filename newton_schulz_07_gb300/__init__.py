@@ -10,6 +10,9 @@ from .ns import (  # noqa: F401
     alloc_workspace,
     launches_per_call,
     muon_ns,
+    muon_ns_f32,
+    f32_workspace_region,
+    f32_workspace_size,
     muon_ns_gram,
     muon_ns_grouped,
     grouped_workspace_size,

@@ -43,6 +43,9 @@ SIGNATURES = {
     "muon_ns_workspace_region": (_c_int, [_c_int, _c_int, _c_int, _c_int, _psz, _psz]),
     "muon_ns_ws": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp]),
+    "muon_ns_f32_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _psz]),
+    "muon_ns_f32_workspace_region": (_c_int, [_c_int, _c_int, _c_int, _c_int, _psz, _psz]),
+    "muon_ns_ws_f32": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_grouped_workspace_size": (_c_int, [_pst, _c_int, _psz]),
     "muon_ns_grouped": (_c_int, [_pst, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),

@@ -28,9 +28,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32 = false>
 cudaError_t launch_tc_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
-  constexpr int kSmem = Staging<SYM, EPI_WARPS>::kSmemBytes;
+  constexpr int kSmem = Staging<SYM, EPI_WARPS, F32>::kSmemBytes;
   // The dynamic shared-memory limit is raised once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -38,12 +38,12 @@ cudaError_t launch_tc_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS>,
+    e = cudaFuncSetAttribute(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS, F32>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  return launch_pdl(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS>, dim3(grid), dim3(Epi<EPI_WARPS>::kCtaThreads),
+  return launch_pdl(ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS, F32>, dim3(grid), dim3(Epi<EPI_WARPS>::kCtaThreads),
                     kSmem, stream, p);
 }
 

@@ -61,12 +61,29 @@ constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
 constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
-constexpr int kPipeBytes = kStages * kStageBytes;
-// Output staging: each epilogue warp stages 32 x 32 bf16 chunks (2 KB, rows
-// of 64 bytes, 64-byte TMA swizzle) that a bulk tensor store writes out.
-constexpr int kChunkBytes = 32 * 32 * 2;
+// Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
+// rows of 64 bytes, 64-byte TMA swizzle; fp32: 4 KB, 128-byte rows and swizzle)
+// that bulk tensor stores write out.
 constexpr int kMnChunk = 64;                   // MN elements per 128-byte row
 constexpr int kMnChunkBytes = kMnChunk * kBlockK * 2;  // 8 KB
+
+// Per element type: bf16 operands (kind::f16 MMA, K = 16 per instruction) or
+// fp32 operands read as tf32 (kind::tf32, K = 8).  A stage always holds one
+// 128-byte swizzle row of K per operand row: 64 bf16 or 32 fp32, so a stage is
+// 48 KB either way; the fp32 variant keeps 3 stages to leave shared memory for
+// its 4 KB output chunks.
+template <bool F32>
+struct ElemCfg {
+  static constexpr int kBytes = F32 ? 4 : 2;
+  static constexpr int kBlockK = 128 / kBytes;                    // K per stage
+  static constexpr int kMmaK = F32 ? 8 : 16;                      // K per tcgen05.mma
+  static constexpr int kStages = F32 ? 3 : 4;
+  static constexpr int kMnChunk = 128 / kBytes;                   // MN elements per 128-byte row
+  static constexpr int kMnChunkBytes = kMnChunk * kBlockK * kBytes;  // 8 KB or 4 KB
+  static constexpr int kMnStep = kMmaK * 128;  // bytes between MMA K steps, MN-major
+  static constexpr int kChunkBytes = 32 * 32 * kBytes;            // 32 x 32 output chunk
+  static constexpr int kAddVec = 32 * kBytes / 16;                 // 16-byte vectors per chunk row
+};
 
 // Epilogue warps: 4 or 8, i.e. one or two per TMEM lane quarter.  The
 // symmetric products (mirrored stores) always take 8; the update takes 8 when
@@ -84,10 +101,11 @@ struct Epi {
 // Staging buffers per epilogue warp: symmetric products need two at once
 // (the chunk and its transpose); the update double-buffers with 4 warps and
 // single-buffers with 8 (shared-memory budget).
-template <bool SYM, int EPI_WARPS>
+template <bool SYM, int EPI_WARPS, bool F32 = false>
 struct Staging {
   static constexpr int kBufs = SYM ? 2 : (EPI_WARPS == 4 ? 2 : 1);
-  static constexpr int kSmemBytes = kPipeBytes + EPI_WARPS * kBufs * kChunkBytes + 1024;  // + align
+  static constexpr int kSmemBytes = ElemCfg<F32>::kStages * kStageBytes +
+                                    EPI_WARPS * kBufs * ElemCfg<F32>::kChunkBytes + 1024;  // + align
 };
 
 // Byte offset of element (row, col) of a 32 x 32 bf16 staging chunk: rows of
@@ -96,6 +114,22 @@ struct Staging {
 __device__ __forceinline__ uint32_t stage_off(int row, int col) {
   const int g = (col >> 3) ^ ((row >> 1) & 3);
   return static_cast<uint32_t>(row * 64 + g * 16 + (col & 7) * 2);
+}
+
+// The same for a 32 x 32 fp32 chunk: rows of 128 bytes, granule XOR (row & 7)
+// (the 128-byte TMA swizzle).
+__device__ __forceinline__ uint32_t stage_off32(int row, int col) {
+  const int g = (col >> 2) ^ (row & 7);
+  return static_cast<uint32_t>(row * 128 + g * 16 + (col & 3) * 4);
+}
+
+// Round an fp32 value to the nearest tf32 (10-bit mantissa, ties to even),
+// kept in fp32 storage: the tensor core reads tf32 by dropping the low 13
+// bits, so values stored this way reach it exactly.  Inputs here are finite.
+__device__ __forceinline__ uint32_t round_tf32_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0xFFFu + ((u >> 13) & 1u);
+  return u & 0xFFFFE000u;
 }
 
 // A launch covers up to kMaxGroups stacks ("groups") of same-shape matrices,
@@ -108,7 +142,7 @@ struct GroupArgs {
   TileSpace space;
   int M, N, K;           // output rows, output columns, contraction length
   int num_kb;            // ceil(K / kBlockK)
-  const uint16_t* addend;  // bf16 [batch][M][N] with row stride ld, or nullptr
+  const void* addend;    // [batch][M][N] (bf16, or fp32 for F32) with row stride ld, or nullptr
   long long ld;
   long long bstride;
   // Diagonal kept in fp32 (both optional):
@@ -135,6 +169,7 @@ struct GemmParams {
   long long total_tiles;
   float alpha, beta, eps;
   int diag_per_col;
+  int round_tf32;     // F32 only: store outputs rounded to tf32 (they feed an MMA)
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -200,9 +235,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
+  using EC = ElemCfg<F32>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
   __shared__ uint32_t tmem_base_sh;
@@ -283,26 +319,26 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           ptx::mbar_arrive_expect_tx(sy.full(stage), kStageBytes);
           const uint32_t sa = smem_base + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
-          const int k0 = kb * kBlockK;
+          const int k0 = kb * EC::kBlockK;
           if (A_MN) {
 #pragma unroll
-            for (int c = 0; c < kTileM / kMnChunk; ++c)
-              ptx::tma_load_3d(sa + c * kMnChunkBytes, tmA, sy.full(stage), row0 + c * kMnChunk,
-                               k0, b);
+            for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
+              ptx::tma_load_3d(sa + c * EC::kMnChunkBytes, tmA, sy.full(stage),
+                               row0 + c * EC::kMnChunk, k0, b);
           } else {
             ptx::tma_load_3d(sa, tmA, sy.full(stage), k0, row0, b);
           }
           if (B_MN) {
 #pragma unroll
-            for (int c = 0; c < kTileN / kMnChunk; ++c)
-              ptx::tma_load_3d(sb + c * kMnChunkBytes, tmB, sy.full(stage), col0 + c * kMnChunk,
-                               k0, b);
+            for (int c = 0; c < kTileN / EC::kMnChunk; ++c)
+              ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, tmB, sy.full(stage),
+                               col0 + c * EC::kMnChunk, k0, b);
           } else {
             ptx::tma_load_3d(sb, tmB, sy.full(stage), k0, col0, b);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == EC::kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -311,14 +347,16 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       }
       // Wait for every copy still in flight before the CTA can exit.
 #pragma unroll
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < EC::kStages; ++s)
         if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, P.budget);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_full = ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
-      constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
+      constexpr uint32_t idesc_full = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN, A_MN, B_MN)
+                                          : ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
+      constexpr uint32_t idesc_half = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN / 2, A_MN, B_MN)
+                                          : ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -350,15 +388,22 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           const uint32_t sa = smem_base + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            const uint64_t ad = A_MN ? ptx::sw128_desc(sa + kk * 2048, kMnChunkBytes, 1024)
-                                     : ptx::sw128_desc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::sw128_desc(sb + kk * 2048, kMnChunkBytes, 1024)
-                                     : ptx::sw128_desc(sb + kk * 32, 16, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
+            // K-major: an MMA's K slice is 32 bytes further along the swizzle
+            // row; MN-major: kMmaK k-rows of 128 bytes further down.
+            const uint64_t ad =
+                A_MN ? ptx::sw128_desc(sa + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                     : ptx::sw128_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd =
+                B_MN ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                     : ptx::sw128_desc(sb + kk * 32, 16, 1024);
+            if (F32)
+              ptx::mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(sy.empty(stage));
-          if (++stage == kStages) {
+          if (++stage == EC::kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -381,8 +426,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const int c_begin = (e >> 2) * kChunksPerWarp;
     const int r_in_tile = q * 32 + lane;
     float* colc = colc_sh[SYM ? 0 : e];
-    constexpr int kBufs = Staging<SYM, EPI_WARPS>::kBufs;
-    const uint32_t stg = smem_base + kPipeBytes + static_cast<uint32_t>(e * kBufs * kChunkBytes);
+    constexpr int kBufs = Staging<SYM, EPI_WARPS, F32>::kBufs;
+    constexpr int kCB = EC::kChunkBytes;
+    constexpr int kAV = EC::kAddVec;  // 16-byte addend vectors per lane and chunk
+    const uint32_t stg = smem_base + EC::kStages * kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
     int buf = 0;
     uint32_t tphase = 0;
     for (long long t = blockIdx.x; t < total; t += gridDim.x) {
@@ -402,8 +449,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const long long gi = static_cast<long long>(I) * kTileM + r_in_tile;
       const int warp_row_max = I * kTileM + q * 32 + 31;
       const bool row_ok = gi < G.M;
-      const uint16_t* addm =
-          G.addend ? G.addend + static_cast<long long>(b) * G.bstride : nullptr;
+      const uint8_t* addm =
+          G.addend ? static_cast<const uint8_t*>(G.addend) + static_cast<long long>(b) * G.bstride * EC::kBytes
+                   : nullptr;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * kTileN);
       const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
@@ -427,19 +475,25 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         }
         __syncwarp();
       }
-      // Addend values of one chunk (16-byte groups of 8 bf16), prefetched one
-      // chunk ahead so their latency overlaps the previous chunk's work.
-      auto load_addend = [&](int cc, uint4 (&dst)[4]) {
+      // Addend values of one chunk (kAV 16-byte vectors of 8 bf16 or 4 fp32),
+      // prefetched one chunk ahead so their latency overlaps the previous
+      // chunk's work.
+      constexpr int kPer = 16 / EC::kBytes;  // elements per 16-byte vector
+      auto load_addend = [&](int cc, uint4 (&dst)[kAV]) {
         const int gj0 = col_base + cc * 32;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
+        for (int g = 0; g < kAV; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
         if (addm == nullptr || !row_ok || gj0 >= G.N || (SYM && gj0 > gi)) return;
-        const uint4* src = reinterpret_cast<const uint4*>(addm + gi * G.ld + gj0);
+        const uint4* src = reinterpret_cast<const uint4*>(addm + (gi * G.ld + gj0) * EC::kBytes);
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          if (gj0 + 8 * g + 8 <= G.N) dst[g] = __ldg(src + g);
+        for (int g = 0; g < kAV; ++g)
+          if (gj0 + kPer * g + kPer <= G.N) dst[g] = __ldg(src + g);
       };
-      uint4 av[4];
+      // Staging-chunk offset of element (row, col) for this element type.
+      auto soff = [](int row, int col) -> uint32_t {
+        return F32 ? stage_off32(row, col) : stage_off(row, col);
+      };
+      uint4 av[kAV];
       load_addend(0, av);
 
 #pragma unroll 1
@@ -447,7 +501,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int gj0 = col_base + cc * 32;
         if (gj0 >= G.N) break;                   // warp-uniform
         if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
-        uint4 an[4];
+        uint4 an[kAV];
         if (cc + 1 < kChunksPerWarp) load_addend(cc + 1, an);
         uint32_t v[32];
         ptx::tmem_ld_32cols(t_lane + static_cast<uint32_t>((c_begin + cc) * 32), v);
@@ -457,25 +511,33 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = alpha_t * __uint_as_float(v[j]);
         if (addm != nullptr) {
-          const uint32_t ws[16] = {av[0].x, av[0].y, av[0].z, av[0].w, av[1].x, av[1].y,
-                                   av[1].z, av[1].w, av[2].x, av[2].y, av[2].z, av[2].w,
-                                   av[3].x, av[3].y, av[3].z, av[3].w};
+          float x[32];
+#pragma unroll
+          for (int g = 0; g < kAV; ++g) {
+            const uint32_t w4[4] = {av[g].x, av[g].y, av[g].z, av[g].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (F32) {
+                x[4 * g + h] = __uint_as_float(w4[h]);
+              } else {
+                x[8 * g + 2 * h] = detail::bf16_lo(w4[h]);
+                x[8 * g + 2 * h + 1] = detail::bf16_hi(w4[h]);
+              }
+            }
+          }
           if (col_mode) {
             const float4* cp = reinterpret_cast<const float4*>(colc + cc * 32);
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
               const float4 k4 = cp[h];
-              f[4 * h + 0] = fmaf(k4.x, detail::bf16_lo(ws[2 * h]), f[4 * h + 0]);
-              f[4 * h + 1] = fmaf(k4.y, detail::bf16_hi(ws[2 * h]), f[4 * h + 1]);
-              f[4 * h + 2] = fmaf(k4.z, detail::bf16_lo(ws[2 * h + 1]), f[4 * h + 2]);
-              f[4 * h + 3] = fmaf(k4.w, detail::bf16_hi(ws[2 * h + 1]), f[4 * h + 3]);
+              f[4 * h + 0] = fmaf(k4.x, x[4 * h + 0], f[4 * h + 0]);
+              f[4 * h + 1] = fmaf(k4.y, x[4 * h + 1], f[4 * h + 1]);
+              f[4 * h + 2] = fmaf(k4.z, x[4 * h + 2], f[4 * h + 2]);
+              f[4 * h + 3] = fmaf(k4.w, x[4 * h + 3], f[4 * h + 3]);
             }
           } else {
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-              f[2 * h] = fmaf(row_coef, detail::bf16_lo(ws[h]), f[2 * h]);
-              f[2 * h + 1] = fmaf(row_coef, detail::bf16_hi(ws[h]), f[2 * h + 1]);
-            }
+            for (int j = 0; j < 32; ++j) f[j] = fmaf(row_coef, x[j], f[j]);
           }
         }
         if (SYM && G.diag_out != nullptr && row_ok && gi >= gj0 && gi < gj0 + 32) {
@@ -490,9 +552,29 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           }
           G.diag_out[static_cast<long long>(b) * G.M + gi] = dval;
         }
-        uint32_t hv[16];
+        // Output words: 32 fp32 (rounded to tf32 when they feed an MMA) or 16
+        // pairs of bf16; ew(j) is element j as raw bits.
+        constexpr int kW = F32 ? 32 : 16;
+        uint32_t w[kW];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) hv[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
+        for (int h = 0; h < kW; ++h) {
+          if (F32)
+            w[h] = P.round_tf32 ? round_tf32_bits(f[h]) : __float_as_uint(f[h]);
+          else
+            w[h] = detail::pack_bf16x2(f[2 * h], f[2 * h + 1]);
+        }
+        auto st_elem = [&](uint32_t addr, int j) {
+          if (F32)
+            ptx::st_shared_u32(addr, w[j]);
+          else
+            ptx::st_shared_u16(addr, static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+        };
+        auto st_row = [&](uint32_t d) {  // this lane's row of the chunk, 16 bytes at a time
+#pragma unroll
+          for (int g = 0; g < kW / 4; ++g)
+            ptx::st_shared_v4(d + soff(lane, g * kPer), w[4 * g], w[4 * g + 1], w[4 * g + 2],
+                              w[4 * g + 3]);
+        };
         // Stage the chunk in shared memory and write it with bulk tensor
         // stores (rows beyond M or columns beyond N are clipped by the TMA).
         const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
@@ -502,11 +584,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         }
         __syncwarp();
         if (!SYM) {
-          const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kChunkBytes);
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            ptx::st_shared_v4(d + stage_off(lane, 8 * g), hv[4 * g], hv[4 * g + 1], hv[4 * g + 2],
-                              hv[4 * g + 3]);
+          const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kCB);
+          st_row(d);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -516,15 +595,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         } else if (gj0 < R0) {
           // Below the diagonal: the chunk at (R0, gj0) and its transpose at (gj0, R0).
           const uint32_t d = stg;
-          const uint32_t tr = stg + kChunkBytes;
+          const uint32_t tr = stg + kCB;
+          st_row(d);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            ptx::st_shared_v4(d + stage_off(lane, 8 * g), hv[4 * g], hv[4 * g + 1], hv[4 * g + 2],
-                              hv[4 * g + 3]);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            ptx::st_shared_u16(tr + stage_off(j, lane),
-                               static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+          for (int j = 0; j < 32; ++j) st_elem(tr + soff(j, lane), j);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -538,9 +612,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           const uint32_t d = stg;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const uint16_t hj = static_cast<uint16_t>((hv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-            if (j <= lane) ptx::st_shared_u16(d + stage_off(lane, j), hj);
-            if (j < lane) ptx::st_shared_u16(d + stage_off(j, lane), hj);
+            if (j <= lane) st_elem(d + soff(lane, j), j);
+            if (j < lane) st_elem(d + soff(j, lane), j);
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
@@ -550,7 +623,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           }
         }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) av[g] = an[g];
+        for (int g = 0; g < kAV; ++g) av[g] = an[g];
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(sy.tempty(buf));

@@ -19,4 +19,10 @@ cudaError_t launch_sym_mnmn(const GemmParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_full_kmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
 cudaError_t launch_full_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
 
+// The same for fp32 operands and outputs (tf32 tensor cores).
+cudaError_t launch_sym_kk_f32(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_sym_mnmn_f32(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_full_kmn_f32(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk_f32(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
+
 }  // namespace mns

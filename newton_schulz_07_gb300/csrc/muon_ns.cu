@@ -34,7 +34,8 @@ constexpr long long kWaitBudgetCycles = 4000000000LL;  // about 2 s at 2 GHz
 
 struct Problem {
   long long batch, R, C, m, n;
-  bool T;  // rows > cols: the input is kept tall (Y = X^T)
+  bool T;    // rows > cols: the input is kept tall (Y = X^T)
+  bool f32;  // fp32 stacks and iterates (tf32 tensor cores) instead of bf16
 };
 
 struct Layout {
@@ -54,6 +55,7 @@ int check_shape(long long batch, long long rows, long long cols, Problem* p, boo
   p->R = rows;
   p->C = cols;
   p->T = rows > cols;
+  p->f32 = false;
   p->m = p->T ? cols : rows;
   p->n = p->T ? rows : cols;
   *empty = batch == 0 || rows == 0 || cols == 0;
@@ -62,7 +64,8 @@ int check_shape(long long batch, long long rows, long long cols, Problem* p, boo
 
 Layout make_layout(const Problem& p) {
   Layout L;
-  const long long vec = p.R * p.C / 8;
+  const size_t eb = p.f32 ? 4 : 2;  // bytes per element of G, X, A, B
+  const long long vec = p.R * p.C / (p.f32 ? 4 : 8);
   L.chunks = static_cast<int>((vec + mns::kNormChunkVec - 1) / mns::kNormChunkVec);
   if (L.chunks < 1) L.chunks = 1;
   size_t off = 0;
@@ -77,10 +80,10 @@ Layout make_layout(const Problem& p) {
   L.diag = off;
   off = round_up(off + 4 * static_cast<size_t>(p.batch) * p.m, 1024);
   L.x = off;
-  L.x_bytes = 2 * static_cast<size_t>(p.batch) * p.R * p.C;
+  L.x_bytes = eb * static_cast<size_t>(p.batch) * p.R * p.C;
   off = round_up(off + L.x_bytes, 1024);
   L.a = off;
-  L.a_bytes = 2 * static_cast<size_t>(p.batch) * p.m * p.m;
+  L.a_bytes = eb * static_cast<size_t>(p.batch) * p.m * p.m;
   off = round_up(off + L.a_bytes, 1024);
   L.b = off;
   off = round_up(off + L.a_bytes, 1024);
@@ -143,22 +146,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return g_encode;
 }
 
-// 3-D bf16 map over a stack [batch][rows][inner] (inner contiguous) with a
-// box of box_inner x box_rows x 1; 128-byte swizzle for operand tiles, 64-byte
-// swizzle for the 32 x 32 output chunks.
+// 3-D map over a bf16 (or fp32) stack [batch][rows][inner] (inner
+// contiguous) with a box of box_inner x box_rows x 1; 128-byte swizzle for
+// operand tiles, 64-byte (bf16) or 128-byte (fp32) for 32 x 32 output chunks.
 bool make_map(CUtensorMap* map, const void* base, long long inner, long long rows,
-              long long batch, int box_inner, int box_rows,
+              long long batch, int box_inner, int box_rows, bool f32 = false,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const long long eb = f32 ? 4 : 2;
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(batch)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * 2),
-                           static_cast<cuuint64_t>(inner * rows * 2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * eb),
+                           static_cast<cuuint64_t>(inner * rows * eb)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
-      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+      fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+         const_cast<void*>(base), dims, strides, box,
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -166,10 +171,17 @@ bool make_map(CUtensorMap* map, const void* base, long long inner, long long row
 
 // ---------------------------------------------------------------- launches --
 
-// Output map: [batch][M][N] bf16, 32 x 32 boxes, 64-byte swizzle.
-bool make_out_map(CUtensorMap* map, const void* base, long long M, long long N, long long batch) {
-  return make_map(map, base, N, M, batch, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+// Output map: [batch][M][N], 32 x 32 boxes; 64-byte swizzle for bf16 (rows of
+// 64 bytes), 128-byte for fp32.
+bool make_out_map(CUtensorMap* map, const void* base, long long M, long long N, long long batch,
+                  bool f32) {
+  return make_map(map, base, N, M, batch, 32, 32, f32,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
+
+// K per pipeline stage and M/N elements per 128-byte row (the TMA box sizes).
+inline int block_k(bool f32) { return f32 ? mns::ElemCfg<true>::kBlockK : mns::ElemCfg<false>::kBlockK; }
+inline int mn_chunk(bool f32) { return f32 ? mns::ElemCfg<true>::kMnChunk : mns::ElemCfg<false>::kMnChunk; }
 
 int grid_for(long long tiles, int sms) {
   const long long g = tiles < sms ? tiles : sms;
@@ -204,7 +216,7 @@ mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err
 }
 
 void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M, long long N,
-               long long K, long long* total) {
+               long long K, long long* total, bool f32) {
   mns::GroupArgs& G = P->grp[i];
   G.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
                                  static_cast<int>(N));
@@ -213,7 +225,7 @@ void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M,
   G.M = static_cast<int>(M);
   G.N = static_cast<int>(N);
   G.K = static_cast<int>(K);
-  G.num_kb = static_cast<int>((K + mns::kBlockK - 1) / mns::kBlockK);
+  G.num_kb = static_cast<int>((K + block_k(f32) - 1) / block_k(f32));
   G.ld = N;
   G.bstride = M * N;
 }
@@ -221,68 +233,78 @@ void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M,
 int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_t st) {
   mns::GemmParams* P = new_params(ng, 1.0f, 0.0f, eps, err);
   long long total = 0;
-  const bool T = io[0].p.T;
+  const bool T = io[0].p.T, f32 = io[0].p.f32;
+  const int bk = block_k(f32), mc = mn_chunk(f32);
+  P->round_tf32 = 1;  // A feeds the next product
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
-    set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total);
+    set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32);
     P->grp[i].norms = io[i].norms;
-    if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch)) return MUON_NS_ERR_CUDA;
+    if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch, f32)) return MUON_NS_ERR_CUDA;
     if (!T) {
       // X [batch][m][n]: rows of X are the K-major operand rows.
-      if (!make_map(&P->tmA[i], io[i].X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
-          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mns::kBlockK, mns::kTileN))
+      if (!make_map(&P->tmA[i], io[i].X, p.n, p.m, p.batch, bk, mns::kTileM, f32) ||
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, bk, mns::kTileN, f32))
         return MUON_NS_ERR_CUDA;
     } else {
       // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
-      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, mns::kMnChunk, mns::kBlockK))
-        return MUON_NS_ERR_CUDA;
+      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, mc, bk, f32)) return MUON_NS_ERR_CUDA;
       P->tmB[i] = P->tmA[i];
     }
   }
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
+  if (f32)
+    return to_status(T ? mns::launch_sym_mnmn_f32(*P, grid, st) : mns::launch_sym_kk_f32(*P, grid, st));
   return to_status(T ? mns::launch_sym_mnmn(*P, grid, st) : mns::launch_sym_kk(*P, grid, st));
 }
 
 int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cudaStream_t st) {
   mns::GemmParams* P = new_params(ng, c, b, 0.0f, err);
   long long total = 0;
+  const bool f32 = io[0].p.f32;
+  const int bk = block_k(f32);
+  P->round_tf32 = 1;  // B feeds the update product
   for (int i = 0; i < ng; ++i) {
     const long long m = io[i].p.m, batch = io[i].p.batch;
-    set_group(P, i, 1, batch, m, m, m, &total);
+    set_group(P, i, 1, batch, m, m, m, &total, f32);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
-    if (!make_map(&P->tmA[i], io[i].A, m, m, batch, mns::kBlockK, mns::kTileM) ||
-        !make_map(&P->tmB[i], io[i].A, m, m, batch, mns::kBlockK, mns::kTileN) ||
-        !make_out_map(&P->tmOut[i], io[i].B, m, m, batch))
+    if (!make_map(&P->tmA[i], io[i].A, m, m, batch, bk, mns::kTileM, f32) ||
+        !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, mns::kTileN, f32) ||
+        !make_out_map(&P->tmOut[i], io[i].B, m, m, batch, f32))
       return MUON_NS_ERR_CUDA;
   }
   P->total_tiles = total;
-  return to_status(mns::launch_sym_kk(*P, grid_for(total, sms), st));
+  const int grid = grid_for(total, sms);
+  return to_status(f32 ? mns::launch_sym_kk_f32(*P, grid, st) : mns::launch_sym_kk(*P, grid, st));
 }
 
-int run_update(const StepIO* io, int ng, float alpha_x, float eps, int* err, int sms,
-               cudaStream_t st) {
+// `round_out`: fp32 mode only, the result feeds another step's products.
+int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_out, int* err,
+               int sms, cudaStream_t st) {
   mns::GemmParams* P = new_params(ng, 1.0f, alpha_x, eps, err);
   long long total = 0;
-  const bool T = io[0].p.T;
+  const bool T = io[0].p.T, f32 = io[0].p.f32;
+  const int bk = block_k(f32), mc = mn_chunk(f32);
   int max_k = 0;
   P->diag_per_col = T ? 1 : 0;  // (a + D_i) scales row i of X, or column i of Y
+  P->round_tf32 = round_out ? 1 : 0;
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
     if (!T) {
       // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
-      set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total);
-      if (!make_map(&P->tmA[i], io[i].B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileM) ||
-          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mns::kMnChunk, mns::kBlockK) ||
-          !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch))
+      set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total, f32);
+      if (!make_map(&P->tmA[i], io[i].B, p.m, p.m, p.batch, bk, mns::kTileM, f32) ||
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mc, bk, f32) ||
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch, f32))
         return MUON_NS_ERR_CUDA;
     } else {
       // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
-      set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total);
-      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, mns::kBlockK, mns::kTileM) ||
-          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, mns::kBlockK, mns::kTileN) ||
-          !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch))
+      set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total, f32);
+      if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, bk, mns::kTileM, f32) ||
+          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, mns::kTileN, f32) ||
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch, f32))
         return MUON_NS_ERR_CUDA;
     }
     P->grp[i].addend = io[i].X;
@@ -292,24 +314,27 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, int* err, int
   }
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
+  if (f32)
+    return to_status(T ? mns::launch_full_kk_f32(*P, max_k, grid, st)
+                       : mns::launch_full_kmn_f32(*P, max_k, grid, st));
   return to_status(T ? mns::launch_full_kk(*P, max_k, grid, st)
                      : mns::launch_full_kmn(*P, max_k, grid, st));
 }
 
-int run_normalize(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* X, float eps,
+int run_normalize(const Problem& p, const Layout& L, const void* G, void* X, float eps,
                   uint8_t* ws, cudaStream_t st) {
-  const long long vec = p.R * p.C / 8;
+  const long long vec = p.R * p.C / (p.f32 ? 4 : 8);
   if (cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
-  if (mns::launch_pdl(mns::ns_norm_partial, grid, dim3(mns::kNormThreads), 0, st,
+  if (mns::launch_pdl(p.f32 ? mns::ns_norm_partial<true> : mns::ns_norm_partial<false>, grid, dim3(mns::kNormThreads), 0, st,
                       reinterpret_cast<const uint4*>(G), vec, L.chunks,
                       reinterpret_cast<float*>(ws + L.partials),
                       reinterpret_cast<unsigned int*>(ws + L.tickets),
                       reinterpret_cast<float*>(ws + L.norms)) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   if (X == nullptr) return MUON_NS_OK;  // norms only
-  if (mns::launch_pdl(mns::ns_scale, grid, dim3(mns::kNormThreads), 0, st,
+  if (mns::launch_pdl(p.f32 ? mns::ns_scale<true> : mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, st,
                       reinterpret_cast<const uint4*>(G), reinterpret_cast<uint4*>(X), vec,
                       reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
@@ -375,7 +400,8 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
         if (ng == 0) continue;
         if ((s = run_gram(io, ng, eps, err, sms, st)) != MUON_NS_OK) return s;
         if ((s = run_poly(io, ng, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-        if ((s = run_update(io, ng, abc[0], eps, err, sms, st)) != MUON_NS_OK) return s;
+        if ((s = run_update(io, ng, abc[0], eps, k + 1 < steps, err, sms, st)) != MUON_NS_OK)
+          return s;
         for (int j = 0; j < ng; ++j) S[members[j]].cur = io[j].Xn;
       }
     }
@@ -465,13 +491,14 @@ int muon_ns_workspace_size(int batch, int rows, int cols, size_t* bytes) {
   return MUON_NS_OK;
 }
 
-int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* offset,
-                             size_t* bytes) {
+int workspace_region(bool f32, int batch, int rows, int cols, int region, size_t* offset,
+                     size_t* bytes) {
   if (!offset || !bytes) return MUON_NS_ERR_INVALID_ARG;
   Problem p;
   bool empty;
   const int s = check_shape(batch, rows, cols, &p, &empty);
   if (s != MUON_NS_OK) return s;
+  p.f32 = f32;
   const Layout L = make_layout(p);
   switch (region) {
     case MUON_NS_WS_TOTAL: *offset = 0; *bytes = L.total; break;
@@ -483,6 +510,27 @@ int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* 
     case MUON_NS_WS_DIAG: *offset = L.diag; *bytes = 4 * static_cast<size_t>(p.batch) * p.m; break;
     default: return MUON_NS_ERR_INVALID_ARG;
   }
+  return MUON_NS_OK;
+}
+
+int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* offset,
+                             size_t* bytes) {
+  return workspace_region(false, batch, rows, cols, region, offset, bytes);
+}
+
+int muon_ns_f32_workspace_region(int batch, int rows, int cols, int region, size_t* offset,
+                                 size_t* bytes) {
+  return workspace_region(true, batch, rows, cols, region, offset, bytes);
+}
+
+int muon_ns_f32_workspace_size(int batch, int rows, int cols, size_t* bytes) {
+  if (!bytes) return MUON_NS_ERR_INVALID_ARG;
+  Problem p;
+  bool empty;
+  const int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  p.f32 = true;
+  *bytes = empty ? 0 : make_layout(p).total;
   return MUON_NS_OK;
 }
 
@@ -504,6 +552,28 @@ int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
   return run_ns(p, L, G, out, steps, abc, eps, static_cast<uint8_t*>(workspace), d.sms, stream);
+}
+
+int muon_ns_ws_f32(const float* G, float* out, int batch, int rows, int cols, int steps,
+                   const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  p.f32 = true;
+  float abc[3];
+  if ((s = check_scalars(steps, coeffs, eps, abc)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!G || !out) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(out)) return MUON_NS_ERR_ALIGNMENT;
+  const Layout L = make_layout(p);
+  if (!workspace || workspace_bytes < L.total) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return run_ns(p, L, reinterpret_cast<const uint16_t*>(G), reinterpret_cast<uint16_t*>(out), steps,
+                abc, eps, static_cast<uint8_t*>(workspace), d.sms, stream);
 }
 
 int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
@@ -720,7 +790,7 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, mu
   io.D = const_cast<float*>(diag);
   io.norms = norms;
   io.Xn = Xn;
-  return run_update(&io, 1, a, eps, device_error, d.sms, stream);
+  return run_update(&io, 1, a, eps, false, device_error, d.sms, stream);
 }
 
 int muon_ns_launches_per_call(int steps) {

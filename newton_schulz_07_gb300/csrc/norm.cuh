@@ -14,6 +14,7 @@
 //                    in any stack.
 //   ns_scale         grid (chunks, batch): X = bf16_rn(G * (1 / (nu + eps))),
 //                    elementwise in the input orientation (G may equal X).
+// Both are templated on F32: stacks of fp32 (the fp32 NS mode) instead of bf16.
 //
 // The norm is the per-matrix Frobenius normalisation of Dion's dense NS named
 // by prime-rl PR #3873, Summary item 1.
@@ -46,6 +47,12 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 w) {
   return s;
 }
 
+__device__ __forceinline__ float sumsq_f32x4(const uint4 w) {
+  const float a = __uint_as_float(w.x), b = __uint_as_float(w.y);
+  const float c = __uint_as_float(w.z), d = __uint_as_float(w.w);
+  return fmaf(d, d, fmaf(c, c, fmaf(b, b, a * a)));
+}
+
 __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
@@ -63,6 +70,8 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* red) {
 
 }  // namespace detail
 
+// F32: the stack holds fp32 (4 per 16-byte vector) instead of bf16 (8).
+template <bool F32>
 __global__ void __launch_bounds__(kNormThreads)
     ns_norm_partial(const uint4* __restrict__ G, long long vec_per_matrix, int chunks,
                     float* __restrict__ partials, unsigned int* __restrict__ tickets,
@@ -83,7 +92,8 @@ __global__ void __launch_bounds__(kNormThreads)
   }
   float acc = 0.0f;
 #pragma unroll
-  for (int it = 0; it < kNormVecPerThread; ++it) acc += detail::sumsq_bf16x8(w[it]);
+  for (int it = 0; it < kNormVecPerThread; ++it)
+    acc += F32 ? detail::sumsq_f32x4(w[it]) : detail::sumsq_bf16x8(w[it]);
 
   const float part = detail::block_sum_fixed(acc, red);
   if (threadIdx.x == 0) {
@@ -102,6 +112,7 @@ __global__ void __launch_bounds__(kNormThreads)
   if (threadIdx.x == 0) norms[b] = sqrtf(total);
 }
 
+template <bool F32>
 __global__ void __launch_bounds__(kNormThreads)
     ns_scale(const uint4* G, uint4* X, long long vec_per_matrix, const float* __restrict__ norms,
              float eps) {
@@ -125,10 +136,14 @@ __global__ void __launch_bounds__(kNormThreads)
     uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      const float lo = __uint_as_float(ws[h] << 16) * s;
-      const float hi = __uint_as_float(ws[h] & 0xFFFF0000u) * s;
-      ws[h] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+      if (F32) {
+        ws[h] = __float_as_uint(__uint_as_float(ws[h]) * s);
+      } else {
+        const float lo = __uint_as_float(ws[h] << 16) * s;
+        const float hi = __uint_as_float(ws[h] & 0xFFFF0000u) * s;
+        ws[h] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+      }
     }
     x[i] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
   }

@@ -224,3 +224,34 @@ def muon_ns_grouped(Gs, outs=None, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: f
                                               _ptr(workspace), workspace.numel(), _stream(dev)),
                    "muon_ns_grouped")
     return outs
+
+
+def f32_workspace_size(batch: int, rows: int, cols: int) -> int:
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_f32_workspace_size(batch, rows, cols, ctypes.byref(n)), "muon_ns_f32_workspace_size")
+    return n.value
+
+
+def f32_workspace_region(batch: int, rows: int, cols: int, region: int) -> tuple[int, int]:
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_f32_workspace_region(batch, rows, cols, region, ctypes.byref(off),
+                                                       ctypes.byref(nb)), "muon_ns_f32_workspace_region")
+    return off.value, nb.value
+
+
+def muon_ns_f32(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS,
+                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 Newton-Schulz of an fp32 matrix or (batch, rows, cols) stack (tf32
+    tensor cores, fp32 storage); `out` may be G."""
+    if not isinstance(G, torch.Tensor) or G.dtype != torch.float32 or not G.is_cuda or not G.is_contiguous():
+        raise TypeError("G must be a contiguous CUDA float32 tensor")
+    b, r, c = _shape3(G)
+    out = torch.empty_like(G) if out is None else out
+    if out.dtype != torch.float32 or out.shape != G.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor shaped like G")
+    if workspace is None:
+        workspace = torch.empty(max(f32_workspace_size(b, r, c), 1), dtype=torch.uint8, device=G.device)
+    with torch.cuda.device(G.device):
+        _lib.check(_lib.lib().muon_ns_ws_f32(_ptr(G), _ptr(out), b, r, c, int(steps), _coeffs(coeffs), float(eps),
+                                             _ptr(workspace), workspace.numel(), _stream(G.device)), "muon_ns_ws_f32")
+    return out

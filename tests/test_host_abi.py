@@ -266,3 +266,15 @@ def test_grouped_workspace_is_sum_of_stack_workspaces():
                              None) == _lib.ERR_INVALID_ARG
     arr[1] = _lib.MuonNSStack(4096, 4096, 2, 264, 136)
     assert L.muon_ns_grouped(arr, len(shapes), 5, None, 1e-7, ctypes.c_void_p(4096), 16, None) == _lib.ERR_WORKSPACE
+
+
+def test_f32_workspace_regions_hold_fp32():
+    n = ctypes.c_size_t(0)
+    assert _lib.lib().muon_ns_f32_workspace_size(4, 256, 512, ctypes.byref(n)) == _lib.OK
+    assert ns.f32_workspace_region(4, 256, 512, _lib.WS_X)[1] == 4 * 256 * 512 * 4
+    assert ns.f32_workspace_region(4, 256, 512, _lib.WS_GRAM)[1] == 4 * 256 * 256 * 4
+    assert ns.f32_workspace_region(4, 256, 512, _lib.WS_TOTAL)[1] == n.value > _ws(4, 256, 512)[1]
+    L = _lib.lib()
+    p = ctypes.c_void_p(4096)
+    assert L.muon_ns_ws_f32(p, p, 1, 12, 16, 5, None, 1e-7, p, 1 << 30, None) == _lib.ERR_ALIGNMENT
+    assert L.muon_ns_ws_f32(p, p, 1, 16, 16, 5, None, 1e-7, p, 16, None) == _lib.ERR_WORKSPACE
