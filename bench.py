@@ -406,6 +406,7 @@ def main():
             if name == w.name:
                 continue
             per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
+        per_shape[w.name + "_fp32_mode"] = time_f32(torch, ns, w, dev, peaks)
         mixed = [ns_inputs.WORKLOADS["stack_32x7168x2048"], ns_inputs.WORKLOADS["stack_128x2048x768"]]
         per_shape["mixed_stacks_32x7168x2048+128x2048x768"] = time_grouped(torch, ns, mixed, dev, peaks)
 
@@ -481,6 +482,37 @@ def time_workload(torch, ns, w, dev, peaks, steps=10, warmup=3):
     if w.name in PAGES_H200_QUACK_MS:
         res["pages_h200_quack_ms"] = PAGES_H200_QUACK_MS[w.name]
     del G, out, ws, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_f32(torch, ns, w, dev, peaks, steps=10, warmup=3):
+    """The fp32 NS mode (tf32 tensor cores, fp32 storage) on workload w, with
+    matrix 0's error against the fp64 oracle."""
+    x = np.stack([ns_inputs.matrix_f32(w, k) for k in range(w.batch)])
+    G = torch.from_numpy(x).to(dev)
+    out = torch.empty_like(G)
+    ws = torch.empty(ns.f32_workspace_size(w.batch, w.rows, w.cols), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        ns.muon_ns_f32(G, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        ns.muon_ns_f32(G, out=out, workspace=ws)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    import oracle
+    ref = oracle.newton_schulz(x[0].astype(np.float64))
+    err = float(np.linalg.norm(out[0].double().cpu().numpy() - ref) / np.linalg.norm(ref))
+    tf = w.dense_flops() / (ms * 1e-3) / 1e12
+    res = {"ms": ms, "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
+           "mode": "fp32 in/out, tf32 tensor cores", "rel_fro_err_matrix0_vs_fp64_oracle": err,
+           "steps": steps, "l2": f"working set >> L2 ({w.name})", "device_error_word": ns.read_error(ws)}
+    del G, out, ws
     torch.cuda.empty_cache()
     return res
 
