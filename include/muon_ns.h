@@ -146,7 +146,10 @@ int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, i
  * rounded to tf32 (10-bit mantissa, round to nearest even) and multiplied on
  * the tf32 tensor cores with fp32 accumulation; the epilogues, B's diagonal
  * and the final output are full fp32.  About 7x closer to the exact result
- * than the bf16 path, at about twice its time and memory.  Same argument
+ * than the bf16 path, at about twice its time and memory.  Every tensor-core
+ * operand is read K-major here: the iterate is kept in both orientations (the
+ * update also writes its transpose), and the first step makes one transposed
+ * copy of G.  Same argument
  * rules as the bf16 calls (rows and cols multiples of 8, 16-byte aligned
  * pointers, out == G allowed).
  * ------------------------------------------------------------------------- */

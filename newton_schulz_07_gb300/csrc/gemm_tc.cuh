@@ -103,7 +103,9 @@ struct Epi {
 // single-buffers with 8 (shared-memory budget).
 template <bool SYM, int EPI_WARPS, bool F32 = false>
 struct Staging {
-  static constexpr int kBufs = SYM ? 2 : (EPI_WARPS == 4 ? 2 : 1);
+  // fp32 updates may also store their transpose (GemmParams::tmOutT), which
+  // needs both buffers at once, like the symmetric products.
+  static constexpr int kBufs = (SYM || F32) ? 2 : (EPI_WARPS == 4 ? 2 : 1);
   static constexpr int kSmemBytes = ElemCfg<F32>::kStages * kStageBytes +
                                     EPI_WARPS * kBufs * ElemCfg<F32>::kChunkBytes + 1024;  // + align
 };
@@ -164,12 +166,17 @@ struct GemmParams {
   CUtensorMap tmA[kMaxGroups];    // A operand (rows of the output)
   CUtensorMap tmB[kMaxGroups];    // B operand (columns of the output)
   CUtensorMap tmOut[kMaxGroups];  // output, 32 x 32 boxes, 64-byte swizzle
+  // FULL only, optional: the transposed output [batch][N][M] (same boxes),
+  // written when out_t != 0.  The fp32 path keeps its iterate in both
+  // orientations so that every tensor-core operand is K-major.
+  CUtensorMap tmOutT[kMaxGroups];
   GroupArgs grp[kMaxGroups];
   int num_groups;
   long long total_tiles;
   float alpha, beta, eps;
   int diag_per_col;
   int round_tf32;     // F32 only: store outputs rounded to tf32 (they feed an MMA)
+  int out_t;          // FULL only: also write the transposed output through tmOutT
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -436,6 +443,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const int gr = find_group(P, t);
       const GroupArgs& G = P.grp[gr];
       const CUtensorMap* tmOut = &P.tmOut[gr];
+      const CUtensorMap* tmOutT = &P.tmOutT[gr];
       int b, I, J;
       tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
       int ready = 0;
@@ -579,11 +587,26 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // stores (rows beyond M or columns beyond N are clipped by the TMA).
         const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
         if (lane == 0) {
-          if (kBufs == 2 && !SYM) ptx::bulk_wait_read<1>();
+          if (kBufs == 2 && !SYM && !P.out_t) ptx::bulk_wait_read<1>();
           else ptx::bulk_wait_read<0>();
         }
         __syncwarp();
-        if (!SYM) {
+        if (!SYM && P.out_t) {
+          // The chunk at (R0, gj0) and its transpose at (gj0, R0) of the
+          // transposed output.
+          const uint32_t d = stg;
+          const uint32_t tr = stg + kCB;
+          st_row(d);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) st_elem(tr + soff(j, lane), j);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
+            ptx::tma_store_3d(tmOutT, tr, R0, gj0, b);
+            ptx::bulk_commit();
+          }
+        } else if (!SYM) {
           const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kCB);
           st_row(d);
           ptx::fence_proxy_async_smem();

@@ -40,6 +40,7 @@ struct Problem {
 
 struct Layout {
   size_t error, tickets, partials, norms, diag, x, a, b, total;
+  size_t y2, w;  // fp32 mode only: a second tall-orientation iterate and the wide copy
   size_t x_bytes, a_bytes;
   int chunks;
 };
@@ -87,6 +88,12 @@ Layout make_layout(const Problem& p) {
   off = round_up(off + L.a_bytes, 1024);
   L.b = off;
   off = round_up(off + L.a_bytes, 1024);
+  L.y2 = L.w = off;
+  if (p.f32) {
+    off = round_up(off + L.x_bytes, 1024);
+    L.w = off;
+    off = round_up(off + L.x_bytes, 1024);
+  }
   L.total = off;
   return L;
 }
@@ -200,6 +207,7 @@ struct StepIO {
   float* D;            // fp32 diagonal of B
   const float* norms;  // non-null in the first step: X is unscaled
   uint16_t* Xn;        // update output
+  uint16_t* Xt;        // update only, optional: the transposed output
 };
 
 // Launch parameters (about 4 KB) are built on the host and copied at launch.
@@ -290,6 +298,7 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   int max_k = 0;
   P->diag_per_col = T ? 1 : 0;  // (a + D_i) scales row i of X, or column i of Y
   P->round_tf32 = round_out ? 1 : 0;
+  P->out_t = io[0].Xt != nullptr ? 1 : 0;
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
     if (!T) {
@@ -310,6 +319,10 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     P->grp[i].addend = io[i].X;
     P->grp[i].diag_in = io[i].D;
     P->grp[i].norms = io[i].norms;
+    // Transposed output: [batch][N][M] of this launch's [batch][M][N] output.
+    if (io[i].Xt != nullptr &&
+        !make_out_map(&P->tmOutT[i], io[i].Xt, T ? p.m : p.n, T ? p.n : p.m, p.batch, f32))
+      return MUON_NS_ERR_CUDA;
     if (p.m > max_k) max_k = static_cast<int>(p.m);
   }
   P->total_tiles = total;
@@ -388,6 +401,7 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
           else
             nxt = (t.cur == t.out) ? wsx : t.out;
           StepIO& e = io[ng];
+          e = StepIO{};  // every optional field (norms, Xt) starts null
           e.p = t.p;
           e.X = (k == 0) ? t.G : t.cur;
           e.A = reinterpret_cast<uint16_t*>(t.ws + t.L.a);
@@ -411,6 +425,81 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
         cudaMemcpyAsync(S[i].out, S[i].cur, S[i].L.x_bytes, cudaMemcpyDeviceToDevice, st) !=
             cudaSuccess)
       return MUON_NS_ERR_CUDA;
+  return MUON_NS_OK;
+}
+
+// fp32 NS.  The tf32 tensor-core path takes K-major operands only, so the
+// iterate is kept in both orientations: W = the wide m x n copy, read by the
+// Gram product A = W W^T, and Y = W^T (n x m), which the update reads as
+// Y' = a Y + Y B with K-major operands and whose epilogue also writes W' = Y'^T.
+// The first step gets the orientation of G it lacks from one transpose.
+int run_ns_f32(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, int steps,
+               const float abc[3], float eps, uint8_t* ws, int sms, cudaStream_t st) {
+  int* err = reinterpret_cast<int*>(ws + L.error);
+  if (cudaMemsetAsync(ws + L.error, 0, 256, st) != cudaSuccess) return MUON_NS_ERR_CUDA;
+  if (steps == 0) return run_normalize(p, L, G, out, eps, ws, st);
+  int s = run_normalize(p, L, G, nullptr, eps, ws, st);
+  if (s != MUON_NS_OK) return s;
+  uint16_t* Y0 = reinterpret_cast<uint16_t*>(ws + L.x);
+  uint16_t* Y1 = reinterpret_cast<uint16_t*>(ws + L.y2);
+  uint16_t* W = reinterpret_cast<uint16_t*>(ws + L.w);
+  const bool wide = !p.T;
+  // G^T into the orientation G lacks.
+  {
+    const dim3 grid(static_cast<unsigned>((p.C + 31) / 32), static_cast<unsigned>((p.R + 31) / 32),
+                    static_cast<unsigned>(p.batch));
+    if (mns::launch_pdl(mns::ns_transpose_f32, grid, dim3(32, 8), 0, st,
+                        reinterpret_cast<const float*>(G), reinterpret_cast<float*>(wide ? Y0 : W),
+                        static_cast<int>(p.R), static_cast<int>(p.C)) != cudaSuccess)
+      return MUON_NS_ERR_CUDA;
+  }
+  Problem pw = p;  // the Gram sees W: m x n, wide
+  pw.R = p.m;
+  pw.C = p.n;
+  pw.T = false;
+  Problem py = p;  // the update sees Y: n x m, tall
+  py.R = p.n;
+  py.C = p.m;
+  py.T = true;
+  const uint16_t* wsrc = wide ? G : W;
+  const uint16_t* ysrc = wide ? Y0 : G;
+  uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
+  uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
+  float* D = reinterpret_cast<float*>(ws + L.diag);
+  const float* norms = reinterpret_cast<const float*>(ws + L.norms);
+  for (int k = 0; k < steps; ++k) {
+    const bool last = k + 1 == steps;
+    StepIO g = {};
+    g.p = pw;
+    g.X = wsrc;
+    g.A = A;
+    g.norms = k == 0 ? norms : nullptr;
+    if ((s = run_gram(&g, 1, eps, err, sms, st)) != MUON_NS_OK) return s;
+    StepIO q = {};
+    q.p = pw;
+    q.A = A;
+    q.B = B;
+    q.D = D;
+    if ((s = run_poly(&q, 1, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
+    // Y' never overwrites the Y it reads; for a tall input the last Y' is the
+    // result (straight into out unless out is G, still read in step 1).
+    uint16_t* ynext = (ysrc == Y0) ? Y1 : Y0;
+    if (last && !wide && (out != G || k > 0)) ynext = out;
+    StepIO u = {};
+    u.p = py;
+    u.X = ysrc;
+    u.B = B;
+    u.D = D;
+    u.norms = k == 0 ? norms : nullptr;
+    u.Xn = ynext;
+    u.Xt = last ? (wide ? out : nullptr) : W;
+    if ((s = run_update(&u, 1, abc[0], eps, !last, err, sms, st)) != MUON_NS_OK) return s;
+    ysrc = ynext;
+    wsrc = W;
+  }
+  if (!wide && ysrc != out &&
+      cudaMemcpyAsync(out, ysrc, L.x_bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
   return MUON_NS_OK;
 }
 
@@ -572,8 +661,8 @@ int muon_ns_ws_f32(const float* G, float* out, int batch, int rows, int cols, in
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
   DevInfo d;
   if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
-  return run_ns(p, L, reinterpret_cast<const uint16_t*>(G), reinterpret_cast<uint16_t*>(out), steps,
-                abc, eps, static_cast<uint8_t*>(workspace), d.sms, stream);
+  return run_ns_f32(p, L, reinterpret_cast<const uint16_t*>(G), reinterpret_cast<uint16_t*>(out),
+                    steps, abc, eps, static_cast<uint8_t*>(workspace), d.sms, stream);
 }
 
 int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,

@@ -149,4 +149,30 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
+// out[b][c][r] = in[b][r][c] for fp32 stacks [batch][R][C], through a padded
+// 32 x 33 shared tile (coalesced reads and writes).  grid (ceil(C/32),
+// ceil(R/32), batch), block (32, 8).  The fp32 NS path uses it once per call
+// to give the first step both orientations of G.
+__global__ void __launch_bounds__(256)
+    ns_transpose_f32(const float* __restrict__ in, float* __restrict__ out, int R, int C) {
+  __shared__ float tile[32][33];
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
+  const long long mat = static_cast<long long>(R) * C;
+  const float* src = in + blockIdx.z * mat;
+  float* dst = out + blockIdx.z * mat;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int r = r0 + threadIdx.y + k, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[threadIdx.y + k][threadIdx.x] = src[static_cast<long long>(r) * C + c];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int c = c0 + threadIdx.y + k, r = r0 + threadIdx.x;
+    if (r < R && c < C) dst[static_cast<long long>(c) * R + r] = tile[threadIdx.x][threadIdx.y + k];
+  }
+}
+
 }  // namespace mns
