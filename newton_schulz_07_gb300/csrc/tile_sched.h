@@ -11,7 +11,11 @@
 // row tile I (128 rows) and column tile J (256 columns) are needed iff some
 // (i, j) with j <= i lies in the tile, i.e. J <= floor(I / 2).  Rows 2p and
 // 2p+1 each hold p + 1 tiles, so rows 0..2p-1 hold p (p + 1) tiles; when the
-// number of row tiles is odd the last row (I = 2T - 1) does not exist.
+// number of row tiles is odd the last row (I = 2T - 1) does not exist.  The
+// triangle is walked in groups of kGroupT row tiles, column-major inside a
+// group, so CTAs running at the same time read a band of A-operand rows and a
+// limited set of B-operand column panels (the operand of a large matrix
+// would otherwise be re-streamed from DRAM by every wave).
 //
 // Full grid (update product): groups of kGroupM row tiles are walked
 // column-major inside the group, so CTAs running at the same time share
@@ -32,6 +36,10 @@ namespace mns {
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kGroupM = 8;
+#ifndef MNS_TRI_GROUP
+#define MNS_TRI_GROUP 16
+#endif
+constexpr int kGroupT = MNS_TRI_GROUP;  // row tiles per group of the triangle walk
 
 MNS_HD int ceil_div_i(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -55,6 +63,36 @@ MNS_HD void tri_decode(long long u, int* I, int* J) {
   } else {
     *I = static_cast<int>(2 * p + 1);
     *J = static_cast<int>(v - (p + 1));
+  }
+}
+
+// Tiles in row tiles [0, x) of the triangle: x = 2p -> p (p + 1), x = 2p + 1 -> (p + 1)^2.
+MNS_HD long long tri_rows_tiles(long long x) {
+  const long long p = x / 2;
+  return (x & 1) ? (p + 1) * (p + 1) : p * (p + 1);
+}
+
+// Local triangle index u -> (I, J), grouped walk (groups of kGroupT row tiles,
+// column-major inside a group).
+MNS_HD void tri_decode_grouped(long long u, int tiles_m, int* I, int* J) {
+  long long r0 = 0;
+  while (true) {
+    const long long r1 = (r0 + kGroupT < tiles_m) ? r0 + kGroupT : tiles_m;
+    const long long cnt = tri_rows_tiles(r1) - tri_rows_tiles(r0);
+    if (u < cnt || r1 >= tiles_m) {
+      for (long long j = 0;; ++j) {
+        const long long first = (2 * j > r0) ? 2 * j : r0;
+        const long long n = r1 - first;
+        if (u < n) {
+          *I = static_cast<int>(first + u);
+          *J = static_cast<int>(j);
+          return;
+        }
+        u -= n;
+      }
+    }
+    u -= cnt;
+    r0 = r1;
   }
 }
 
@@ -93,7 +131,7 @@ MNS_HD void tile_decode(const TileSpace& s, long long t, int* b, int* I, int* J)
   const long long u = t - bb * s.per_matrix;
   *b = static_cast<int>(bb);
   if (s.sym)
-    tri_decode(u, I, J);
+    tri_decode_grouped(u, s.tiles_m, I, J);
   else
     grid_decode(u, s.tiles_m, s.tiles_n, I, J);
 }
