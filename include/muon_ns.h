@@ -287,9 +287,12 @@ int muon_ns_launches_per_call(int steps);
 
 /* Persistent tile scheduler of the tensor-core kernels.  kind 0 = lower
  * triangle of an m x m output (M == N), kind 1 = full M x N output.  Tiles are
- * 128 x 256.  muon_ns_tile_count() returns the number of tiles of a launch
- * (-1 on bad arguments); muon_ns_tile_coords() maps a linear tile index to
- * (matrix, row tile, column tile) exactly as the kernels do. */
+ * 128 x 256.  kinds 2 and 3 are the same spaces walked by clusters of two
+ * CTAs: a unit is a pair of row tiles (2p, 2p + 1) of one column tile, and
+ * row_tile returns p.  muon_ns_tile_count() returns the number of units of a
+ * launch (-1 on bad arguments); muon_ns_tile_coords() maps a linear unit
+ * index to (matrix, row tile or pair row, column tile) exactly as the kernels
+ * do. */
 long long muon_ns_tile_count(int kind, int batch, int M, int N);
 int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* matrix,
                         int* row_tile, int* col_tile);

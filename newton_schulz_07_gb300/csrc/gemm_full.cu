@@ -5,13 +5,13 @@
 namespace mns {
 
 cudaError_t launch_full_kmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream) {
-  return max_k <= 1024 ? launch_tc_gemm<false, true, false, 8>(p, grid, stream)
-                       : launch_tc_gemm<false, true, false, 4>(p, grid, stream);
+  return max_k <= 1024 ? launch_tc_gemm<false, true, false, 8, false, kClusterFull>(p, grid, stream)
+                       : launch_tc_gemm<false, true, false, 4, false, kClusterFull>(p, grid, stream);
 }
 
 cudaError_t launch_full_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream) {
-  return max_k <= 1024 ? launch_tc_gemm<false, false, false, 8>(p, grid, stream)
-                       : launch_tc_gemm<false, false, false, 4>(p, grid, stream);
+  return max_k <= 1024 ? launch_tc_gemm<false, false, false, 8, false, kClusterFull>(p, grid, stream)
+                       : launch_tc_gemm<false, false, false, 4, false, kClusterFull>(p, grid, stream);
 }
 
 }  // namespace mns

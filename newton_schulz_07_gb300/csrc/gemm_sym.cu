@@ -5,11 +5,11 @@
 namespace mns {
 
 cudaError_t launch_sym_kk(const GemmParams& p, int grid, cudaStream_t stream) {
-  return launch_tc_gemm<false, false, true, 8>(p, grid, stream);
+  return launch_tc_gemm<false, false, true, 8, false, kClusterSym>(p, grid, stream);
 }
 
 cudaError_t launch_sym_mnmn(const GemmParams& p, int grid, cudaStream_t stream) {
-  return launch_tc_gemm<true, true, true, 8>(p, grid, stream);
+  return launch_tc_gemm<true, true, true, 8, false, kClusterSym>(p, grid, stream);
 }
 
 }  // namespace mns

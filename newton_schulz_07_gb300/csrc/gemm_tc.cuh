@@ -19,7 +19,12 @@
 //   SYM   the output is symmetric: only lower-triangle tiles are scheduled and
 //         every value with j <= i is written to (i, j) and to (j, i), so the
 //         stored matrix is bit-symmetric (one triangle computed and mirrored,
-//         prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381, Summary).
+//         prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381, Summary);
+//   CL    CTAs per cluster, 1 or 2.  With 2, the two CTAs of a cluster compute
+//         row tiles 2p and 2p + 1 of the same column tile, whose B-operand
+//         panel they share: each loads one half of it with a multicast TMA
+//         copy into both CTAs' shared memory, and each MMA commit releases the
+//         stage in both CTAs.  Half the B-operand bytes per CTA come from L2.
 //
 // Uses (m <= n internally; Y = the tall input kept in its own orientation):
 //   Gram X X^T       <false, false, true>   both operands = rows of X
@@ -242,9 +247,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
+  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   using EC = ElemCfg<F32>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
@@ -258,6 +264,12 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &abort_sh;
+  // Units of the tile space are walked with a static stride: one unit per
+  // CTA, or per cluster of two (CTA rank r then takes row tile 2p + r).
+  const uint32_t crank = CL == 2 ? ptx::cluster_ctarank() : 0u;
+  const long long unit0 = CL == 2 ? static_cast<long long>(ptx::cluster_id_x()) : blockIdx.x;
+  const long long ustride = CL == 2 ? static_cast<long long>(ptx::cluster_count_x()) : gridDim.x;
+  auto row_tile = [&](int u) { return CL == 2 ? 2 * u + static_cast<int>(crank) : u; };
 
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   detail::Sync sy;
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(sy.full(s), 1);
-      ptx::mbar_init(sy.empty(s), 1);
+      ptx::mbar_init(sy.empty(s), CL);  // one MMA commit per CTA of the cluster
     }
     ptx::mbar_init(sy.tfull(0), 1);
     ptx::mbar_init(sy.tfull(1), 1);
@@ -289,6 +301,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // The peer CTA's copies and commits target this CTA's barriers: both must
+  // be initialised before either CTA issues one.
+  if (CL == 2) ptx::cluster_sync();
   const uint32_t tmem_base = tmem_base_sh;
   // Every CTA is resident from the start (one per SM), so the next kernel may
   // be scheduled now: its CTAs take SMs as ours exit and finish their prologue
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0;   // stages with a load issued at least once
       uint32_t issued_phase = 0;  // parity of the last load issued per stage
-      for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+      for (long long t = unit0; t < total; t += ustride) {
         const int gr = find_group(P, t);
         const GroupArgs& G = P.grp[gr];
         const CUtensorMap* tmA = &P.tmA[gr];
@@ -314,6 +329,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int num_kb = G.num_kb;
         int b, I, J;
         tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
+        I = row_tile(I);
         const int row0 = I * kTileM;
         const int col0 = J * kTileN;
         bool ok = true;
@@ -335,9 +351,23 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           } else {
             ptx::tma_load_3d(sa, tmA, sy.full(stage), k0, row0, b);
           }
-          if (B_MN) {
+          constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
+          if (CL == 2) {
+            // This CTA's half of the shared panel, into both CTAs.
+            if (B_MN) {
 #pragma unroll
-            for (int c = 0; c < kTileN / EC::kMnChunk; ++c)
+              for (int c = 0; c < kNch / 2; ++c) {
+                const int cg = static_cast<int>(crank) * (kNch / 2) + c;
+                ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, tmB, sy.full(stage),
+                                    col0 + cg * EC::kMnChunk, k0, b, 0x3);
+              }
+            } else {
+              ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), tmB, sy.full(stage), k0,
+                                  col0 + static_cast<int>(crank) * (kTileN / 2), b, 0x3);
+            }
+          } else if (B_MN) {
+#pragma unroll
+            for (int c = 0; c < kNch; ++c)
               ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, tmB, sy.full(stage),
                                col0 + c * EC::kMnChunk, k0, b);
           } else {
@@ -356,6 +386,18 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 #pragma unroll
       for (int s = 0; s < EC::kStages; ++s)
         if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, P.budget);
+      if (CL == 2) {
+        // The peer's MMA commits also arrive on this CTA's empty barriers:
+        // wait until both CTAs have released the last fill of every stage (a
+        // stage never filled passes at once).
+        for (int s = 0; s < EC::kStages; ++s) {
+          detail::drain_wait(sy.empty(stage), phase ^ 1u, P.budget);
+          if (++stage == EC::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -368,7 +410,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       uint32_t phase = 0;
       int buf = 0;
       uint32_t tphase = 0;
-      for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+      for (long long t = unit0; t < total; t += ustride) {
         const int gr = find_group(P, t);
         const GroupArgs& G = P.grp[gr];
         const int num_kb = G.num_kb;
@@ -379,6 +421,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         if (SYM) {
           int b, I, J;
           tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
+          I = row_tile(I);
           if ((I & 1) == 0 && J == (I >> 1)) idesc = idesc_half;
         }
         if (!detail::wait_bounded(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
@@ -409,7 +452,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             else
               ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(sy.empty(stage));
+          if (CL == 2)
+            ptx::mma_commit_mc(sy.empty(stage), 0x3);
+          else
+            ptx::mma_commit(sy.empty(stage));
           if (++stage == EC::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -439,13 +485,17 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const uint32_t stg = smem_base + EC::kStages * kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
     int buf = 0;
     uint32_t tphase = 0;
-    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+    for (long long t = unit0; t < total; t += ustride) {
       const int gr = find_group(P, t);
       const GroupArgs& G = P.grp[gr];
       const CUtensorMap* tmOut = &P.tmOut[gr];
       const CUtensorMap* tmOutT = &P.tmOutT[gr];
       int b, I, J;
       tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
+      I = row_tile(I);
+      // A row tile past the last one (second CTA of a cluster, odd row-tile
+      // count) was computed on zero-filled operands: nothing to store.
+      const int n_chunks = (CL == 2 && I * kTileM >= G.M) ? 0 : kChunksPerWarp;
       int ready = 0;
       if (lane == 0)
         ready = detail::wait_bounded(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
@@ -505,7 +555,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       load_addend(0, av);
 
 #pragma unroll 1
-      for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+      for (int cc = 0; cc < n_chunks; ++cc) {
         const int gj0 = col_base + cc * 32;
         if (gj0 >= G.N) break;                   // warp-uniform
         if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
@@ -661,6 +711,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // Neither CTA of a cluster leaves while the other may still address it.
+  if (CL == 2) ptx::cluster_sync();
   if (warp == 0) {
     __syncwarp();
     ptx::tmem_dealloc(tmem_base, kTmemCols);

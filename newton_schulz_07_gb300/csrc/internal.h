@@ -11,6 +11,19 @@ namespace mns {
 
 struct GemmParams;
 
+// CTAs per cluster of the bf16 products (1, or 2 for pairs of row tiles that
+// share their B-operand panel through TMA multicast).  The host builds the
+// tile spaces and the B-operand tensor maps to match.  The fp32 products run
+// without clusters.
+#ifndef MNS_CLUSTER_SYM
+#define MNS_CLUSTER_SYM 2
+#endif
+#ifndef MNS_CLUSTER_FULL
+#define MNS_CLUSTER_FULL 2
+#endif
+constexpr int kClusterSym = MNS_CLUSTER_SYM;
+constexpr int kClusterFull = MNS_CLUSTER_FULL;
+
 // Gram / polynomial products: lower-triangle tiles, mirrored stores.
 cudaError_t launch_sym_kk(const GemmParams& p, int grid, cudaStream_t stream);    // K-major operands
 cudaError_t launch_sym_mnmn(const GemmParams& p, int grid, cudaStream_t stream);  // MN-major operands

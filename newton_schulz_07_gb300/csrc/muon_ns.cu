@@ -223,11 +223,18 @@ mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err
   return &P;
 }
 
+// Clusters of two CTAs (paired tile spaces, half-height B boxes) for the bf16
+// products; the fp32 products run without clusters.
+inline bool paired_sym(bool f32) { return !f32 && mns::kClusterSym == 2; }
+inline bool paired_full(bool f32) { return !f32 && mns::kClusterFull == 2; }
+// Rows of a K-major B-operand box: each CTA of a pair loads half the panel.
+inline int b_box_rows(bool paired) { return paired ? mns::kTileN / 2 : mns::kTileN; }
+
 void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M, long long N,
                long long K, long long* total, bool f32) {
   mns::GroupArgs& G = P->grp[i];
   G.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
-                                 static_cast<int>(N));
+                                 static_cast<int>(N), sym ? paired_sym(f32) : paired_full(f32));
   G.tile_begin = *total;
   *total += G.space.total;
   G.M = static_cast<int>(M);
@@ -252,7 +259,7 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
     if (!T) {
       // X [batch][m][n]: rows of X are the K-major operand rows.
       if (!make_map(&P->tmA[i], io[i].X, p.n, p.m, p.batch, bk, mns::kTileM, f32) ||
-          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, bk, mns::kTileN, f32))
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, bk, b_box_rows(paired_sym(f32)), f32))
         return MUON_NS_ERR_CUDA;
     } else {
       // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
@@ -279,7 +286,7 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
     if (!make_map(&P->tmA[i], io[i].A, m, m, batch, bk, mns::kTileM, f32) ||
-        !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, mns::kTileN, f32) ||
+        !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, b_box_rows(paired_sym(f32)), f32) ||
         !make_out_map(&P->tmOut[i], io[i].B, m, m, batch, f32))
       return MUON_NS_ERR_CUDA;
   }
@@ -312,7 +319,7 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
       // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
       set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total, f32);
       if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, bk, mns::kTileM, f32) ||
-          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, mns::kTileN, f32) ||
+          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, b_box_rows(paired_full(f32)), f32) ||
           !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch, f32))
         return MUON_NS_ERR_CUDA;
     }
@@ -887,9 +894,9 @@ int muon_ns_launches_per_call(int steps) {
 }
 
 long long muon_ns_tile_count(int kind, int batch, int M, int N) {
-  if ((kind != 0 && kind != 1) || batch < 0 || M < 0 || N < 0) return -1;
-  if (kind == 0 && M != N) return -1;
-  return mns::make_tile_space(kind == 0 ? 1 : 0, batch, M, N).total;
+  if (kind < 0 || kind > 3 || batch < 0 || M < 0 || N < 0) return -1;
+  if ((kind & 1) == 0 && M != N) return -1;
+  return mns::make_tile_space((kind & 1) == 0 ? 1 : 0, batch, M, N, kind >> 1).total;
 }
 
 int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* matrix,
@@ -897,7 +904,7 @@ int muon_ns_tile_coords(int kind, int batch, int M, int N, long long tile, int* 
   if (!matrix || !row_tile || !col_tile) return MUON_NS_ERR_INVALID_ARG;
   const long long total = muon_ns_tile_count(kind, batch, M, N);
   if (total < 0 || tile < 0 || tile >= total) return MUON_NS_ERR_INVALID_ARG;
-  const mns::TileSpace sp = mns::make_tile_space(kind == 0 ? 1 : 0, batch, M, N);
+  const mns::TileSpace sp = mns::make_tile_space((kind & 1) == 0 ? 1 : 0, batch, M, N, kind >> 1);
   mns::tile_decode(sp, tile, matrix, row_tile, col_tile);
   return MUON_NS_OK;
 }

@@ -20,9 +20,17 @@
 // Full grid (update product): groups of kGroupM row tiles are walked
 // column-major inside the group, so CTAs running at the same time share
 // operand panels in L2.
+//
+// Paired spaces (kernels launched as clusters of two CTAs that share the
+// B-operand panel of a column tile through TMA multicast): a unit of the
+// space is a pair of row tiles (2p, 2p + 1) with one column tile J; CTA rank r
+// of the cluster computes row tile 2p + r.  For the triangle, both row tiles
+// of a pair hold the column tiles J <= p, so the pairs form the plain lower
+// triangle J <= p of ceil(tiles_m / 2) pair rows.  A row tile 2p + 1 beyond
+// the last row tile (odd tiles_m) is computed on zero-filled operands and
+// not stored.
 #pragma once
 
-#include <cmath>
 #include <cstdint>
 
 #ifdef __CUDACC__
@@ -47,23 +55,6 @@ MNS_HD int ceil_div_i(long long a, long long b) { return static_cast<int>((a + b
 MNS_HD long long tri_tiles(int tiles_m) {
   const long long T = (tiles_m + 1) / 2;
   return (tiles_m & 1) ? T * T : T * (T + 1);
-}
-
-// Local triangle index u -> (I, J).
-MNS_HD void tri_decode(long long u, int* I, int* J) {
-  // p = largest integer with p (p + 1) <= u.
-  long long p = static_cast<long long>((sqrtf(4.0f * static_cast<float>(u) + 1.0f) - 1.0f) * 0.5f);
-  if (p < 0) p = 0;
-  while (p > 0 && p * (p + 1) > u) --p;
-  while ((p + 1) * (p + 2) <= u) ++p;
-  const long long v = u - p * (p + 1);
-  if (v <= p) {
-    *I = static_cast<int>(2 * p);
-    *J = static_cast<int>(v);
-  } else {
-    *I = static_cast<int>(2 * p + 1);
-    *J = static_cast<int>(v - (p + 1));
-  }
 }
 
 // Tiles in row tiles [0, x) of the triangle: x = 2p -> p (p + 1), x = 2p + 1 -> (p + 1)^2.
@@ -96,44 +87,85 @@ MNS_HD void tri_decode_grouped(long long u, int tiles_m, int* I, int* J) {
   }
 }
 
+// Local index u of the paired triangle (pair rows p, J <= p) -> (p, J),
+// grouped walk (groups of kGroupT / 2 pair rows, column-major inside a group).
+MNS_HD void ptri_decode_grouped(long long u, int pair_rows, int* p, int* J) {
+  constexpr long long kG = kGroupT / 2 > 0 ? kGroupT / 2 : 1;
+  long long r0 = 0;
+  while (true) {
+    const long long r1 = (r0 + kG < pair_rows) ? r0 + kG : pair_rows;
+    const long long cnt = r1 * (r1 + 1) / 2 - r0 * (r0 + 1) / 2;
+    if (u < cnt || r1 >= pair_rows) {
+      for (long long j = 0;; ++j) {
+        const long long first = j > r0 ? j : r0;
+        const long long n = r1 - first;
+        if (u < n) {
+          *p = static_cast<int>(first + u);
+          *J = static_cast<int>(j);
+          return;
+        }
+        u -= n;
+      }
+    }
+    u -= cnt;
+    r0 = r1;
+  }
+}
+
 // Local full-grid index u -> (I, J), grouped raster.
-MNS_HD void grid_decode(long long u, int tiles_m, int tiles_n, int* I, int* J) {
-  const long long per_group = static_cast<long long>(kGroupM) * tiles_n;
+MNS_HD void grid_decode(long long u, int tiles_m, int tiles_n, int* I, int* J,
+                        int group = kGroupM) {
+  const long long per_group = static_cast<long long>(group) * tiles_n;
   const long long g = u / per_group;
   const long long r = u - g * per_group;
-  const long long first = g * kGroupM;
+  const long long first = g * group;
   long long rows = tiles_m - first;
-  if (rows > kGroupM) rows = kGroupM;
+  if (rows > group) rows = group;
   *I = static_cast<int>(first + r % rows);
   *J = static_cast<int>(r / rows);
 }
 
 struct TileSpace {
   int sym;          // 1: lower triangle, 0: full grid
+  int pair;         // 1: units are pairs of row tiles (clusters of two CTAs)
   int tiles_m;      // row tiles per matrix
   int tiles_n;      // column tiles per matrix
-  long long per_matrix;
+  long long per_matrix;  // units per matrix
   long long total;
 };
 
-MNS_HD TileSpace make_tile_space(int sym, int batch, int M, int N) {
+MNS_HD TileSpace make_tile_space(int sym, int batch, int M, int N, int pair = 0) {
   TileSpace s;
   s.sym = sym;
+  s.pair = pair;
   s.tiles_m = ceil_div_i(M, kTileM);
   s.tiles_n = ceil_div_i(N, kTileN);
-  s.per_matrix = sym ? tri_tiles(s.tiles_m) : static_cast<long long>(s.tiles_m) * s.tiles_n;
+  const long long pr = (s.tiles_m + 1) / 2;
+  if (pair)
+    s.per_matrix = sym ? pr * (pr + 1) / 2 : pr * s.tiles_n;
+  else
+    s.per_matrix = sym ? tri_tiles(s.tiles_m) : static_cast<long long>(s.tiles_m) * s.tiles_n;
   s.total = s.per_matrix * batch;
   return s;
 }
 
+// Unit t -> (matrix b, row tile I, column tile J); for a paired space I is
+// the pair row p (the CTAs compute row tiles 2p and 2p + 1).
 MNS_HD void tile_decode(const TileSpace& s, long long t, int* b, int* I, int* J) {
   const long long bb = t / s.per_matrix;
   const long long u = t - bb * s.per_matrix;
   *b = static_cast<int>(bb);
-  if (s.sym)
+  if (s.pair) {
+    const int pr = (s.tiles_m + 1) / 2;
+    if (s.sym)
+      ptri_decode_grouped(u, pr, I, J);
+    else
+      grid_decode(u, pr, s.tiles_n, I, J, kGroupM / 2);
+  } else if (s.sym) {
     tri_decode_grouped(u, s.tiles_m, I, J);
-  else
+  } else {
     grid_decode(u, s.tiles_m, s.tiles_n, I, J);
+  }
 }
 
 }  // namespace mns

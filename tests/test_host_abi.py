@@ -189,6 +189,43 @@ def test_grid_schedule_covers_every_tile_once(M, N):
     assert len(ts) == len(set(ts)) and set(ts) == expect
 
 
+def unpair(units, M):
+    """Row tiles the two CTAs of a cluster compute for paired units (b, p, J):
+    2p and 2p + 1, the latter only if it exists (otherwise nothing is stored)."""
+    tm = -(-M // TILE_M)
+    return [(b, 2 * p + r, J) for b, p, J in units for r in (0, 1) if 2 * p + r < tm]
+
+
+@pytest.mark.parametrize("m", SYM_SIZES)
+def test_paired_triangle_schedule_covers_lower_triangle_once(m):
+    ts = unpair(tiles(2, 2, m, m), m)
+    tm = -(-m // TILE_M)
+    T = -(-m // TILE_N)
+    expect = {(b, I, J) for b in range(2) for I in range(tm) for J in range(T) if J <= I // 2}
+    assert len(ts) == len(set(ts)) == len(expect)
+    assert set(ts) == expect
+    assert [b for b, _, _ in ts] == sorted(b for b, _, _ in ts)
+
+
+@pytest.mark.parametrize("M,N", [(8, 8), (128, 256), (136, 264), (1536, 2048), (2048, 768), (400, 1000),
+                                 (1100, 520), (7168, 2048)])
+def test_paired_grid_schedule_covers_every_tile_once(M, N):
+    ts = unpair(tiles(3, 3, M, N), M)
+    tm, tn = -(-M // TILE_M), -(-N // TILE_N)
+    expect = {(b, I, J) for b in range(3) for I in range(tm) for J in range(tn)}
+    assert len(ts) == len(set(ts)) and set(ts) == expect
+
+
+def test_paired_tile_counts():
+    L = _lib.lib()
+    assert L.muon_ns_tile_count(2, 128, 1536, 1536) == 128 * 21  # 6 pair rows: 6 * 7 / 2
+    assert L.muon_ns_tile_count(2, 1, 8192, 8192) == 32 * 33 // 2
+    assert L.muon_ns_tile_count(3, 128, 1536, 2048) == 128 * 6 * 8
+    assert L.muon_ns_tile_count(3, 1, 136, 264) == 1 * 2  # one pair row (row tiles 0, 1), two column tiles
+    assert L.muon_ns_tile_count(2, 1, 16, 8) == -1
+    assert L.muon_ns_tile_count(4, 1, 16, 16) == -1
+
+
 def _epilogue_writes(kind, M, N, ts):
     """Model of the epilogue store predicates: counts how often each output
     element is written (direct and mirrored stores) over all tiles."""
@@ -213,6 +250,7 @@ def _epilogue_writes(kind, M, N, ts):
 def test_symmetric_epilogue_writes_each_element_once(m):
     ts = [t for t in tiles(0, 1, m, m)]
     assert np.all(_epilogue_writes(0, m, m, ts) == 1)
+    assert np.all(_epilogue_writes(0, m, m, unpair(tiles(2, 1, m, m), m)) == 1)
 
 
 @pytest.mark.parametrize("M,N", [(8, 8), (136, 264), (400, 1000)])
