@@ -24,7 +24,13 @@
 //         row tiles 2p and 2p + 1 of the same column tile, whose B-operand
 //         panel they share: each loads one half of it with a multicast TMA
 //         copy into both CTAs' shared memory, and each MMA commit releases the
-//         stage in both CTAs.  Half the B-operand bytes per CTA come from L2.
+//         stage in both CTAs.  Half the B-operand bytes per CTA come from L2;
+//   SM2   (CL == 2 only) the pair runs 2-SM MMAs instead: one thread of CTA 0
+//         issues M = 256 tcgen05.mma.cta_group::2 over A tiles held by both
+//         CTAs (128 rows each) and a B panel split in halves between them,
+//         so each CTA stores and loads only its own half of the panel
+//         (32 KB stages instead of 48 KB, 6 of them); each CTA's TMEM holds
+//         its own 128 rows of the accumulator.
 //
 // Uses (m <= n internally; Y = the tall input kept in its own orientation):
 //   Gram X X^T       <false, false, true>   both operands = rows of X
@@ -61,11 +67,20 @@
 namespace mns {
 
 constexpr int kBlockK = 64;   // K per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
-constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
-constexpr int kBBytes = kTileN * kBlockK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = kTileM * 128;          // A tile: 128 rows of 128 bytes (16 KB)
+constexpr int kBBytes = kTileN * 128;          // B panel: 256 rows of 128 bytes (32 KB)
+constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
+
+// Operand ring of one CTA: a stage holds its A tile and the B rows it keeps
+// (the whole panel, or half of it with 2-SM MMAs).
+template <bool F32, bool SM2>
+struct Ring {
+  static constexpr int kBBytesCta = SM2 ? kBBytes / 2 : kBBytes;
+  static constexpr int kStageBytes = kABytes + kBBytesCta;
+  static constexpr int kStages = SM2 ? 6 : (F32 ? 3 : 4);
+  static_assert(kStages <= kMaxStages, "ring depth");
+};
 // Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
 // rows of 64 bytes, 64-byte TMA swizzle; fp32: 4 KB, 128-byte rows and swizzle)
 // that bulk tensor stores write out.
@@ -82,7 +97,6 @@ struct ElemCfg {
   static constexpr int kBytes = F32 ? 4 : 2;
   static constexpr int kBlockK = 128 / kBytes;                    // K per stage
   static constexpr int kMmaK = F32 ? 8 : 16;                      // K per tcgen05.mma
-  static constexpr int kStages = F32 ? 3 : 4;
   static constexpr int kMnChunk = 128 / kBytes;                   // MN elements per 128-byte row
   static constexpr int kMnChunkBytes = kMnChunk * kBlockK * kBytes;  // 8 KB or 4 KB
   static constexpr int kMnStep = kMmaK * 128;  // bytes between MMA K steps, MN-major
@@ -106,12 +120,12 @@ struct Epi {
 // Staging buffers per epilogue warp: symmetric products need two at once
 // (the chunk and its transpose); the update double-buffers with 4 warps and
 // single-buffers with 8 (shared-memory budget).
-template <bool SYM, int EPI_WARPS, bool F32 = false>
+template <bool SYM, int EPI_WARPS, bool F32 = false, bool SM2 = false>
 struct Staging {
   // fp32 updates may also store their transpose (GemmParams::tmOutT), which
   // needs both buffers at once, like the symmetric products.
   static constexpr int kBufs = (SYM || F32) ? 2 : (EPI_WARPS == 4 ? 2 : 1);
-  static constexpr int kSmemBytes = ElemCfg<F32>::kStages * kStageBytes +
+  static constexpr int kSmemBytes = Ring<F32, SM2>::kStages * Ring<F32, SM2>::kStageBytes +
                                     EPI_WARPS * kBufs * ElemCfg<F32>::kChunkBytes + 1024;  // + align
 };
 
@@ -196,14 +210,14 @@ __device__ __forceinline__ int find_group(const GemmParams& P, long long t) {
 namespace detail {
 
 // Shared-memory addresses of the kernel's mbarriers, laid out consecutively:
-// full[kStages], empty[kStages], tfull[2], tempty[2], mma_done.
+// full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], mma_done.
 struct Sync {
   uint32_t base;
   __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * s; }
-  __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (kStages + s); }
-  __device__ __forceinline__ uint32_t tfull(int i) const { return base + 8u * (2 * kStages + i); }
-  __device__ __forceinline__ uint32_t tempty(int i) const { return base + 8u * (2 * kStages + 2 + i); }
-  __device__ __forceinline__ uint32_t mma_done() const { return base + 8u * (2 * kStages + 4); }
+  __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (kMaxStages + s); }
+  __device__ __forceinline__ uint32_t tfull(int i) const { return base + 8u * (2 * kMaxStages + i); }
+  __device__ __forceinline__ uint32_t tempty(int i) const { return base + 8u * (2 * kMaxStages + 2 + i); }
+  __device__ __forceinline__ uint32_t mma_done() const { return base + 8u * (2 * kMaxStages + 4); }
 };
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag, int* err) {
@@ -211,15 +225,23 @@ __device__ __forceinline__ void raise_error(volatile int* abort_flag, int* err) 
   if (err) atomicOr(err, 1);
 }
 
+// Poll of one mbarrier phase; cluster-scope acquire where another CTA of the
+// cluster arrives on the barrier.
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
 // Bounded wait.  Returns false (and raises the abort flag on expiry) if the
 // phase did not complete within the budget or another role aborted.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, int* err,
                                              long long budget) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (try_wait<CLUSTER>(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait<CLUSTER>(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > budget) {
       raise_error(abort_flag, err);
@@ -229,9 +251,10 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Bounded wait used on the way out: ignores the abort flag.
+template <bool CLUSTER = false>
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
   const long long t0 = clock64();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!try_wait<CLUSTER>(bar, parity)) {
     if (clock64() - t0 > budget) return;
   }
 }
@@ -247,13 +270,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, bool SM2 = false>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
+  static_assert(!SM2 || (CL == 2 && !F32), "2-SM MMAs: bf16 CTA pairs");
   using EC = ElemCfg<F32>;
+  using R = Ring<F32, SM2>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 5];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   constexpr int kEpiWarps = Epi<EPI_WARPS>::kWarps;
@@ -270,6 +295,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   const long long unit0 = CL == 2 ? static_cast<long long>(ptx::cluster_id_x()) : blockIdx.x;
   const long long ustride = CL == 2 ? static_cast<long long>(ptx::cluster_count_x()) : gridDim.x;
   auto row_tile = [&](int u) { return CL == 2 ? 2 * u + static_cast<int>(crank) : u; };
+  // 2-SM MMAs: CTA 0 of the pair issues them and owns the operand-full and
+  // accumulator-empty barriers; both CTAs load their halves and drain their
+  // own TMEM rows.
+  const bool leader = crank == 0;
 
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   detail::Sync sy;
@@ -277,14 +306,18 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < R::kStages; ++s) {
       ptx::mbar_init(sy.full(s), 1);
-      ptx::mbar_init(sy.empty(s), CL);  // one MMA commit per CTA of the cluster
+      // One MMA commit per CTA of a multicast pair; the pair's single commit
+      // with 2-SM MMAs.
+      ptx::mbar_init(sy.empty(s), (CL == 2 && !SM2) ? 2 : 1);
     }
     ptx::mbar_init(sy.tfull(0), 1);
     ptx::mbar_init(sy.tfull(1), 1);
-    ptx::mbar_init(sy.tempty(0), kEpiThreads);
-    ptx::mbar_init(sy.tempty(1), kEpiThreads);
+    // Every epilogue thread arrives; with 2-SM MMAs one lane per epilogue
+    // warp of both CTAs (on CTA 0's barrier).
+    ptx::mbar_init(sy.tempty(0), SM2 ? 2 * kEpiWarps : kEpiThreads);
+    ptx::mbar_init(sy.tempty(1), SM2 ? 2 * kEpiWarps : kEpiThreads);
     ptx::mbar_init(sy.mma_done(), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -294,16 +327,25 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       ptx::prefetch_tensormap(&P.tmOut[g]);
     }
   }
+  // The peer CTA's copies, commits and arrivals target this CTA's barriers:
+  // both must be initialised before either CTA issues one.
+  if (SM2) {
+    __syncthreads();
+    ptx::cluster_sync();
+  }
   if (warp == 0) {
-    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols);
-    ptx::tmem_relinquish();
+    if (SM2) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(&tmem_base_sh), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  // The peer CTA's copies and commits target this CTA's barriers: both must
-  // be initialised before either CTA issues one.
-  if (CL == 2) ptx::cluster_sync();
+  if (CL == 2 && !SM2) ptx::cluster_sync();
   const uint32_t tmem_base = tmem_base_sh;
   // Every CTA is resident from the start (one per SM), so the next kernel may
   // be scheduled now: its CTAs take SMs as ours exit and finish their prologue
@@ -334,15 +376,45 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int col0 = J * kTileN;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.empty(stage), phase ^ 1u, abort_flag, P.err,
-                                    P.budget)) {
+          if (!detail::wait_bounded<SM2>(sy.empty(stage), phase ^ 1u, abort_flag, P.err,
+                                         P.budget)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(sy.full(stage), kStageBytes);
-          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sa = smem_base + stage * R::kStageBytes;
           const uint32_t sb = sa + kABytes;
           const int k0 = kb * EC::kBlockK;
+          constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
+          if (SM2) {
+            // This CTA's A tile and its half of the B panel, into its own
+            // shared memory; all bytes of the pair are counted on CTA 0's
+            // barrier, which expects both CTAs' stages.
+            const uint32_t fb = ptx::mapa(sy.full(stage), 0);
+            if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), 2 * R::kStageBytes);
+            if (A_MN) {
+#pragma unroll
+              for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
+                ptx::tma_load_3d_pair(sa + c * EC::kMnChunkBytes, tmA, fb, row0 + c * EC::kMnChunk, k0, b);
+            } else {
+              ptx::tma_load_3d_pair(sa, tmA, fb, k0, row0, b);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int c = 0; c < kNch / 2; ++c)
+                ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, tmB, fb,
+                                      col0 + (static_cast<int>(crank) * (kNch / 2) + c) * EC::kMnChunk, k0, b);
+            } else {
+              ptx::tma_load_3d_pair(sb, tmB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
+            }
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == R::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          ptx::mbar_arrive_expect_tx(sy.full(stage), R::kStageBytes);
           if (A_MN) {
 #pragma unroll
             for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
@@ -351,7 +423,6 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           } else {
             ptx::tma_load_3d(sa, tmA, sy.full(stage), k0, row0, b);
           }
-          constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
           if (CL == 2) {
             // This CTA's half of the shared panel, into both CTAs.
             if (B_MN) {
@@ -375,24 +446,28 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == EC::kStages) {
+          if (++stage == R::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
       }
-      // Wait for every copy still in flight before the CTA can exit.
+      // Wait for every copy still in flight before the CTA can exit (with
+      // 2-SM MMAs CTA 0's barriers count the copies of both CTAs).
+      if (!SM2 || leader) {
 #pragma unroll
-      for (int s = 0; s < EC::kStages; ++s)
-        if (issued_mask & (1u << s)) detail::drain_wait(sy.full(s), (issued_phase >> s) & 1u, P.budget);
+        for (int s = 0; s < R::kStages; ++s)
+          if (issued_mask & (1u << s))
+            detail::drain_wait<SM2>(sy.full(s), (issued_phase >> s) & 1u, P.budget);
+      }
       if (CL == 2) {
-        // The peer's MMA commits also arrive on this CTA's empty barriers:
-        // wait until both CTAs have released the last fill of every stage (a
-        // stage never filled passes at once).
-        for (int s = 0; s < EC::kStages; ++s) {
-          detail::drain_wait(sy.empty(stage), phase ^ 1u, P.budget);
-          if (++stage == EC::kStages) {
+        // The other CTA's MMA commits also arrive on this CTA's empty
+        // barriers: wait until the last fill of every stage has been released
+        // (a stage never filled passes at once).
+        for (int s = 0; s < R::kStages; ++s) {
+          detail::drain_wait<SM2>(sy.empty(stage), phase ^ 1u, P.budget);
+          if (++stage == R::kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -400,10 +475,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!SM2 || leader)) {
       // ---------------------------------------------------------- MMA issuer
+      // (2-SM MMAs: M = 256, the pair's two row tiles at once.)
       constexpr uint32_t idesc_full = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN, A_MN, B_MN)
-                                          : ptx::idesc_bf16_f32(kTileM, kTileN, A_MN, B_MN);
+                                          : ptx::idesc_bf16_f32(SM2 ? 2 * kTileM : kTileM, kTileN, A_MN, B_MN);
       constexpr uint32_t idesc_half = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN / 2, A_MN, B_MN)
                                           : ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
       int stage = 0;
@@ -416,26 +492,27 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int num_kb = G.num_kb;
         // In a symmetric product, a tile on an even row tile I = 2J lies on the
         // diagonal 256-column block with its right half entirely above the
-        // diagonal: only its left 128 columns are computed (N = 128).
+        // diagonal: only its left 128 columns are computed (N = 128).  A 2-SM
+        // MMA shares N between the pair's row tiles and always takes 256.
         uint32_t idesc = idesc_full;
-        if (SYM) {
+        if (SYM && !SM2) {
           int b, I, J;
           tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
           I = row_tile(I);
           if ((I & 1) == 0 && J == (I >> 1)) idesc = idesc_half;
         }
-        if (!detail::wait_bounded(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
+        if (!detail::wait_bounded<SM2>(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded(sy.full(stage), phase, abort_flag, P.err, P.budget)) {
+          if (!detail::wait_bounded<SM2>(sy.full(stage), phase, abort_flag, P.err, P.budget)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sa = smem_base + stage * R::kStageBytes;
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
@@ -449,26 +526,36 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
                      : ptx::sw128_desc(sb + kk * 32, 16, 1024);
             if (F32)
               ptx::mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else if (SM2)
+              ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             else
               ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (CL == 2)
+          if (SM2)
+            ptx::mma_commit_pair(sy.empty(stage), 0x3);
+          else if (CL == 2)
             ptx::mma_commit_mc(sy.empty(stage), 0x3);
           else
             ptx::mma_commit(sy.empty(stage));
-          if (++stage == EC::kStages) {
+          if (++stage == R::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(sy.tfull(buf));
+        if (SM2)
+          ptx::mma_commit_pair(sy.tfull(buf), 0x3);
+        else
+          ptx::mma_commit(sy.tfull(buf));
         buf ^= 1;
         if (buf == 0) tphase ^= 1u;
       }
       // Every MMA issued by this thread has finished once this arrives.
-      ptx::mma_commit(sy.mma_done());
-      detail::drain_wait(sy.mma_done(), 0, P.budget);
+      if (SM2)
+        ptx::mma_commit_pair(sy.mma_done(), 0x1);
+      else
+        ptx::mma_commit(sy.mma_done());
+      detail::drain_wait<SM2>(sy.mma_done(), 0, P.budget);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -479,10 +566,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const int c_begin = (e >> 2) * kChunksPerWarp;
     const int r_in_tile = q * 32 + lane;
     float* colc = colc_sh[SYM ? 0 : e];
-    constexpr int kBufs = Staging<SYM, EPI_WARPS, F32>::kBufs;
+    constexpr int kBufs = Staging<SYM, EPI_WARPS, F32, SM2>::kBufs;
     constexpr int kCB = EC::kChunkBytes;
     constexpr int kAV = EC::kAddVec;  // 16-byte addend vectors per lane and chunk
-    const uint32_t stg = smem_base + EC::kStages * kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
+    const uint32_t stg = smem_base + R::kStages * R::kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
     int buf = 0;
     uint32_t tphase = 0;
     for (long long t = unit0; t < total; t += ustride) {
@@ -498,7 +585,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const int n_chunks = (CL == 2 && I * kTileM >= G.M) ? 0 : kChunksPerWarp;
       int ready = 0;
       if (lane == 0)
-        ready = detail::wait_bounded(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
+        ready = detail::wait_bounded<SM2>(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       __syncwarp();
@@ -699,7 +786,19 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         for (int g = 0; g < kAV; ++g) av[g] = an[g];
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(sy.tempty(buf));
+      if (SM2) {
+        // One arrival per warp, on CTA 0's barrier: the pair's next MMAs
+        // write both CTAs' accumulators.
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            ptx::mbar_arrive(sy.tempty(buf));
+          else
+            ptx::mbar_arrive_remote(ptx::mapa(sy.tempty(buf), 0));
+        }
+      } else {
+        ptx::mbar_arrive(sy.tempty(buf));
+      }
       buf ^= 1;
       if (buf == 0) tphase ^= 1u;
     }
@@ -715,7 +814,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   if (CL == 2) ptx::cluster_sync();
   if (warp == 0) {
     __syncwarp();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if (SM2)
+      ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 

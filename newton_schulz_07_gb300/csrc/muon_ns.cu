@@ -251,8 +251,10 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   const bool T = io[0].p.T, f32 = io[0].p.f32;
   const int bk = block_k(f32), mc = mn_chunk(f32);
   P->round_tf32 = 1;  // A feeds the next product
+  int max_k = 0;
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
+    if (p.n > max_k) max_k = static_cast<int>(p.n);
     set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32);
     P->grp[i].norms = io[i].norms;
     if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch, f32)) return MUON_NS_ERR_CUDA;
@@ -271,7 +273,7 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   const int grid = grid_for(total, sms);
   if (f32)
     return to_status(T ? mns::launch_sym_mnmn_f32(*P, grid, st) : mns::launch_sym_kk_f32(*P, grid, st));
-  return to_status(T ? mns::launch_sym_mnmn(*P, grid, st) : mns::launch_sym_kk(*P, grid, st));
+  return to_status(T ? mns::launch_sym_mnmn(*P, max_k, grid, st) : mns::launch_sym_kk(*P, max_k, grid, st));
 }
 
 int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cudaStream_t st) {
@@ -280,8 +282,10 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
   const bool f32 = io[0].p.f32;
   const int bk = block_k(f32);
   P->round_tf32 = 1;  // B feeds the update product
+  int max_k = 0;
   for (int i = 0; i < ng; ++i) {
     const long long m = io[i].p.m, batch = io[i].p.batch;
+    if (m > max_k) max_k = static_cast<int>(m);
     set_group(P, i, 1, batch, m, m, m, &total, f32);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
@@ -292,7 +296,7 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
   }
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
-  return to_status(f32 ? mns::launch_sym_kk_f32(*P, grid, st) : mns::launch_sym_kk(*P, grid, st));
+  return to_status(f32 ? mns::launch_sym_kk_f32(*P, grid, st) : mns::launch_sym_kk(*P, max_k, grid, st));
 }
 
 // `round_out`: fp32 mode only, the result feeds another step's products.

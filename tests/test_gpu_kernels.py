@@ -5,7 +5,10 @@ Tolerance, from the arithmetic: each kernel rounds its fp32 result to bf16
 once (relative error <= 2^-9 per element, so <= 2^-9 ~ 1.95e-3 in relative
 Frobenius norm) after an fp32 accumulation whose error is far smaller at these
 sizes; the bound used is 3e-3.  Shapes span several 128 x 256 tiles, ragged
-edges in M, N and K, and batches.
+edges in M, N and K, and batches.  Contractions above 1024 run on CTA pairs
+with 2-SM MMAs, shorter ones on pairs sharing a multicast B panel; the
+1096 x 1304 cases also give the pair walk an odd row-tile count (the second
+CTA of the last pair has no rows to store).
 """
 import numpy as np
 import pytest
@@ -20,7 +23,7 @@ pytestmark = pytest.mark.gpu
 KERNEL_TOL = 3e-3
 
 SHAPES = [(1, 8, 8), (3, 136, 264), (2, 256, 512), (2, 264, 136), (1, 392, 200), (1, 200, 392),
-          (2, 128, 128), (1, 520, 1040), (1, 1040, 520)]
+          (2, 128, 128), (1, 520, 1040), (1, 1040, 520), (1, 1096, 1304), (1, 1304, 1096)]
 
 
 def f64(bits):
@@ -61,7 +64,7 @@ def test_gram(shape):
     assert max(per_matrix_rel(f64(a), ref)) <= KERNEL_TOL
 
 
-@pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1040)])
+@pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1040), (2, 1096)])
 @pytest.mark.parametrize("split_diag", [False, True])
 def test_poly(batch, m, split_diag):
     bits = symmetric_bits(batch, m, seed=m)

@@ -48,7 +48,8 @@ def test_tiny_workloads_vs_oracle(name):
 
 
 @pytest.mark.parametrize("shape", [(1, 8, 8), (3, 136, 264), (2, 264, 136), (1, 8, 2048), (1, 2048, 8),
-                                   (2, 40, 24), (1, 392, 392), (2, 520, 1040), (1, 1000, 776)])
+                                   (2, 40, 24), (1, 392, 392), (2, 520, 1040), (1, 1000, 776),
+                                   (1, 1096, 1304), (2, 1304, 1096)])
 def test_ragged_shapes_vs_oracle(shape):
     bits = random_bits(shape, seed=sum(shape))
     out, _ = run_ws(bits)
