@@ -72,15 +72,7 @@ constexpr int kBBytes = kTileN * 128;          // B panel: 256 rows of 128 bytes
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
 
-// Operand ring of one CTA: a stage holds its A tile and the B rows it keeps
-// (the whole panel, or half of it with 2-SM MMAs).
-template <bool F32, bool SM2>
-struct Ring {
-  static constexpr int kBBytesCta = SM2 ? kBBytes / 2 : kBBytes;
-  static constexpr int kStageBytes = kABytes + kBBytesCta;
-  static constexpr int kStages = SM2 ? 6 : (F32 ? 3 : 4);
-  static_assert(kStages <= kMaxStages, "ring depth");
-};
+
 // Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
 // rows of 64 bytes, 64-byte TMA swizzle; fp32: 4 KB, 128-byte rows and swizzle)
 // that bulk tensor stores write out.
@@ -117,16 +109,28 @@ struct Epi {
   static constexpr int kChunksPerWarp = (kTileN / 32) / (kWarps / 4);
 };
 
-// Staging buffers per epilogue warp: symmetric products need two at once
-// (the chunk and its transpose); the update double-buffers with 4 warps and
-// single-buffers with 8 (shared-memory budget).
+// Shared memory of one CTA: the operand ring and the epilogue's staging.
+//   Staging buffers per epilogue warp: symmetric products need two at once
+//   (the chunk and its transpose), and so do fp32 updates that also store
+//   their transpose (GemmParams::tmOutT); the bf16 update double-buffers with
+//   4 warps and single-buffers with 8.
+//   Ring: a stage holds the CTA's A tile and the B rows it keeps, the whole
+//   256-row panel (48 KB) or, with 2-SM MMAs, its 128-row half (32 KB); 4
+//   stages of 48 KB for bf16 and 3 for fp32 (larger staging), and with 2-SM
+//   MMAs as many 32 KB stages as fit, at most 6.
 template <bool SYM, int EPI_WARPS, bool F32 = false, bool SM2 = false>
-struct Staging {
-  // fp32 updates may also store their transpose (GemmParams::tmOutT), which
-  // needs both buffers at once, like the symmetric products.
+struct Smem {
   static constexpr int kBufs = (SYM || F32) ? 2 : (EPI_WARPS == 4 ? 2 : 1);
-  static constexpr int kSmemBytes = Ring<F32, SM2>::kStages * Ring<F32, SM2>::kStageBytes +
-                                    EPI_WARPS * kBufs * ElemCfg<F32>::kChunkBytes + 1024;  // + align
+  static constexpr int kStagingBytes = EPI_WARPS * kBufs * ElemCfg<F32>::kChunkBytes;
+  static constexpr int kStageBytes = kABytes + (SM2 ? kBBytes / 2 : kBBytes);
+  // 227 KB per CTA, less an upper bound of the kernel's static shared memory
+  // (barriers, and the update's per-column coefficients) and 1 KB of alignment.
+  static constexpr int kRingMax = 232448 - (SYM ? 1024 : 4608) - kStagingBytes - 1024;
+  static constexpr int kFit = kRingMax / kStageBytes;
+  static constexpr int kStages = SM2 ? (kFit < 6 ? kFit : 6) : (F32 ? 3 : 4);
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024;
+  static_assert(kStages >= 2 && kStages <= kMaxStages, "ring depth");
+  static_assert(kSmemBytes <= kRingMax + kStagingBytes + 1024, "shared memory");
 };
 
 // Byte offset of element (row, col) of a 32 x 32 bf16 staging chunk: rows of
@@ -275,9 +279,9 @@ template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, b
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
-  static_assert(!SM2 || (CL == 2 && !F32), "2-SM MMAs: bf16 CTA pairs");
+  static_assert(!SM2 || CL == 2, "2-SM MMAs run on CTA pairs");
   using EC = ElemCfg<F32>;
-  using R = Ring<F32, SM2>;
+  using R = Smem<SYM, EPI_WARPS, F32, SM2>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
   __shared__ uint32_t tmem_base_sh;
@@ -479,8 +483,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     if (lane == 0 && (!SM2 || leader)) {
       // ---------------------------------------------------------- MMA issuer
       // (2-SM MMAs: M = 256, the pair's two row tiles at once.)
-      constexpr uint32_t idesc_full = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN, A_MN, B_MN)
-                                          : ptx::idesc_bf16_f32(SM2 ? 2 * kTileM : kTileM, kTileN, A_MN, B_MN);
+      constexpr int kMmaM = SM2 ? 2 * kTileM : kTileM;
+      constexpr uint32_t idesc_full = F32 ? ptx::idesc_tf32_f32(kMmaM, kTileN, A_MN, B_MN)
+                                          : ptx::idesc_bf16_f32(kMmaM, kTileN, A_MN, B_MN);
       constexpr uint32_t idesc_half = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN / 2, A_MN, B_MN)
                                           : ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
       int stage = 0;
@@ -525,7 +530,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             const uint64_t bd =
                 B_MN ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
                      : ptx::sw128_desc(sb + kk * 32, 16, 1024);
-            if (F32)
+            if (F32 && SM2)
+              ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else if (F32)
               ptx::mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             else if (SM2)
               ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -567,7 +574,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const int c_begin = (e >> 2) * kChunksPerWarp;
     const int r_in_tile = q * 32 + lane;
     float* colc = colc_sh[SYM ? 0 : e];
-    constexpr int kBufs = Staging<SYM, EPI_WARPS, F32, SM2>::kBufs;
+    constexpr int kBufs = R::kBufs;
     constexpr int kCB = EC::kChunkBytes;
     constexpr int kAV = EC::kAddVec;  // 16-byte addend vectors per lane and chunk
     const uint32_t stg = smem_base + R::kStages * R::kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);

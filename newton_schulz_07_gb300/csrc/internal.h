@@ -11,42 +11,43 @@ namespace mns {
 
 struct GemmParams;
 
-// CTAs per cluster of the bf16 products (1, or 2 for pairs of row tiles that
-// share their B-operand panel through TMA multicast).  The host builds the
-// tile spaces and the B-operand tensor maps to match.  The fp32 products run
-// without clusters.
-#ifndef MNS_CLUSTER_SYM
-#define MNS_CLUSTER_SYM 2
-#endif
-#ifndef MNS_CLUSTER_FULL
-#define MNS_CLUSTER_FULL 2
-#endif
-// bf16 pairs run 2-SM MMAs when the launch's longest contraction exceeds
-// kPairMmaMinK - 1, and single-CTA MMAs on a multicast B panel otherwise:
-// short contractions leave the epilogue as long as the main loop, and a 2-SM
-// pair must wait for both CTAs' epilogues before reusing an accumulator
-// (measured on GB300: K = 768 products 3-8 % slower with 2-SM MMAs, K >= 1536
-// products 2-11 % faster).  MNS_PAIR_MMA=0 disables 2-SM MMAs.
+// How a product launch pairs its CTAs.  The host builds the tile space and
+// the B-operand tensor maps from the mode, and the launcher instantiates the
+// kernel for it.
+enum PairMode : int {
+  kSingle = 0,     // one CTA per 128 x 256 tile
+  kMulticast = 1,  // clusters of two CTAs (row tiles 2p, 2p + 1) sharing a multicast B panel
+  kPairMma = 2,    // clusters of two CTAs running 2-SM MMAs (M = 256)
+};
+
+// 2-SM MMAs for contractions longer than 1024; shorter ones leave the
+// epilogue as long as the main loop, and a 2-SM pair must wait for both
+// CTAs' epilogues before reusing an accumulator (measured on GB300: K = 768
+// bf16 products 3-8 % slower with 2-SM MMAs, K >= 1536 products 2-11 %
+// faster).  Short bf16 products use multicast pairs; short fp32 products run
+// single CTAs (multicast pairs measured slightly slower for them).
+// MNS_PAIR_MMA=0 turns 2-SM MMAs off.
 #ifndef MNS_PAIR_MMA
 #define MNS_PAIR_MMA 1
 #endif
-constexpr int kClusterSym = MNS_CLUSTER_SYM;
-constexpr int kClusterFull = MNS_CLUSTER_FULL;
-constexpr int kPairMmaMinK = MNS_PAIR_MMA ? 1025 : 0x7FFFFFFF;
+inline PairMode pair_mode(bool f32, int max_k) {
+  if (MNS_PAIR_MMA && max_k > 1024) return kPairMma;
+  return f32 ? kSingle : kMulticast;
+}
 
 // `max_k` is the largest contraction of the launch's groups: short
-// contractions use 8 epilogue warps in the update and no 2-SM MMAs.
+// contractions use 8 epilogue warps in the update.
 // Gram / polynomial products: lower-triangle tiles, mirrored stores.
-cudaError_t launch_sym_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream);    // K-major operands
-cudaError_t launch_sym_mnmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream);  // MN-major operands
+cudaError_t launch_sym_kk(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);    // K-major operands
+cudaError_t launch_sym_mnmn(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);  // MN-major operands
 // Update products: full output grid.
-cudaError_t launch_full_kmn(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
-cudaError_t launch_full_kk(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_full_kmn(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
 
 // The same for fp32 operands and outputs (tf32 tensor cores).
-cudaError_t launch_sym_kk_f32(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_sym_mnmn_f32(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_full_kmn_f32(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
-cudaError_t launch_full_kk_f32(const GemmParams& p, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_sym_kk_f32(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+cudaError_t launch_sym_mnmn_f32(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+cudaError_t launch_full_kmn_f32(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk_f32(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
 
 }  // namespace mns

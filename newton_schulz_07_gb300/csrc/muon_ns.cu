@@ -223,18 +223,14 @@ mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err
   return &P;
 }
 
-// Clusters of two CTAs (paired tile spaces, half-height B boxes) for the bf16
-// products; the fp32 products run without clusters.
-inline bool paired_sym(bool f32) { return !f32 && mns::kClusterSym == 2; }
-inline bool paired_full(bool f32) { return !f32 && mns::kClusterFull == 2; }
 // Rows of a K-major B-operand box: each CTA of a pair loads half the panel.
-inline int b_box_rows(bool paired) { return paired ? mns::kTileN / 2 : mns::kTileN; }
+inline int b_box_rows(mns::PairMode mode) { return mode != mns::kSingle ? mns::kTileN / 2 : mns::kTileN; }
 
 void set_group(mns::GemmParams* P, int i, int sym, long long batch, long long M, long long N,
-               long long K, long long* total, bool f32) {
+               long long K, long long* total, bool f32, mns::PairMode mode) {
   mns::GroupArgs& G = P->grp[i];
   G.space = mns::make_tile_space(sym, static_cast<int>(batch), static_cast<int>(M),
-                                 static_cast<int>(N), sym ? paired_sym(f32) : paired_full(f32));
+                                 static_cast<int>(N), mode != mns::kSingle ? 1 : 0);
   G.tile_begin = *total;
   *total += G.space.total;
   G.M = static_cast<int>(M);
@@ -252,16 +248,18 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   const int bk = block_k(f32), mc = mn_chunk(f32);
   P->round_tf32 = 1;  // A feeds the next product
   int max_k = 0;
+  for (int i = 0; i < ng; ++i)
+    if (io[i].p.n > max_k) max_k = static_cast<int>(io[i].p.n);
+  const mns::PairMode mode = mns::pair_mode(f32, max_k);
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
-    if (p.n > max_k) max_k = static_cast<int>(p.n);
-    set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32);
+    set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32, mode);
     P->grp[i].norms = io[i].norms;
     if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch, f32)) return MUON_NS_ERR_CUDA;
     if (!T) {
       // X [batch][m][n]: rows of X are the K-major operand rows.
       if (!make_map(&P->tmA[i], io[i].X, p.n, p.m, p.batch, bk, mns::kTileM, f32) ||
-          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, bk, b_box_rows(paired_sym(f32)), f32))
+          !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, bk, b_box_rows(mode), f32))
         return MUON_NS_ERR_CUDA;
     } else {
       // Y [batch][n][m]: columns of Y are the operand rows, read MN-major.
@@ -272,8 +270,8 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
   if (f32)
-    return to_status(T ? mns::launch_sym_mnmn_f32(*P, grid, st) : mns::launch_sym_kk_f32(*P, grid, st));
-  return to_status(T ? mns::launch_sym_mnmn(*P, max_k, grid, st) : mns::launch_sym_kk(*P, max_k, grid, st));
+    return to_status(T ? mns::launch_sym_mnmn_f32(*P, mode, grid, st) : mns::launch_sym_kk_f32(*P, mode, grid, st));
+  return to_status(T ? mns::launch_sym_mnmn(*P, mode, grid, st) : mns::launch_sym_kk(*P, mode, grid, st));
 }
 
 int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cudaStream_t st) {
@@ -283,20 +281,22 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
   const int bk = block_k(f32);
   P->round_tf32 = 1;  // B feeds the update product
   int max_k = 0;
+  for (int i = 0; i < ng; ++i)
+    if (io[i].p.m > max_k) max_k = static_cast<int>(io[i].p.m);
+  const mns::PairMode mode = mns::pair_mode(f32, max_k);
   for (int i = 0; i < ng; ++i) {
     const long long m = io[i].p.m, batch = io[i].p.batch;
-    if (m > max_k) max_k = static_cast<int>(m);
-    set_group(P, i, 1, batch, m, m, m, &total, f32);
+    set_group(P, i, 1, batch, m, m, m, &total, f32, mode);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
     if (!make_map(&P->tmA[i], io[i].A, m, m, batch, bk, mns::kTileM, f32) ||
-        !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, b_box_rows(paired_sym(f32)), f32) ||
+        !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, b_box_rows(mode), f32) ||
         !make_out_map(&P->tmOut[i], io[i].B, m, m, batch, f32))
       return MUON_NS_ERR_CUDA;
   }
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
-  return to_status(f32 ? mns::launch_sym_kk_f32(*P, grid, st) : mns::launch_sym_kk(*P, max_k, grid, st));
+  return to_status(f32 ? mns::launch_sym_kk_f32(*P, mode, grid, st) : mns::launch_sym_kk(*P, mode, grid, st));
 }
 
 // `round_out`: fp32 mode only, the result feeds another step's products.
@@ -310,20 +310,23 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   P->diag_per_col = T ? 1 : 0;  // (a + D_i) scales row i of X, or column i of Y
   P->round_tf32 = round_out ? 1 : 0;
   P->out_t = io[0].Xt != nullptr ? 1 : 0;
+  for (int i = 0; i < ng; ++i)
+    if (io[i].p.m > max_k) max_k = static_cast<int>(io[i].p.m);
+  const mns::PairMode mode = mns::pair_mode(f32, max_k);
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
     if (!T) {
       // Xn [m][n] = a X + B X: A operand = rows of B, B operand = X read MN-major.
-      set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total, f32);
+      set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total, f32, mode);
       if (!make_map(&P->tmA[i], io[i].B, p.m, p.m, p.batch, bk, mns::kTileM, f32) ||
           !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mc, bk, f32) ||
           !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch, f32))
         return MUON_NS_ERR_CUDA;
     } else {
       // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
-      set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total, f32);
+      set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total, f32, mode);
       if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, bk, mns::kTileM, f32) ||
-          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, b_box_rows(paired_full(f32)), f32) ||
+          !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, b_box_rows(mode), f32) ||
           !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch, f32))
         return MUON_NS_ERR_CUDA;
     }
@@ -334,15 +337,14 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     if (io[i].Xt != nullptr &&
         !make_out_map(&P->tmOutT[i], io[i].Xt, T ? p.m : p.n, T ? p.n : p.m, p.batch, f32))
       return MUON_NS_ERR_CUDA;
-    if (p.m > max_k) max_k = static_cast<int>(p.m);
   }
   P->total_tiles = total;
   const int grid = grid_for(total, sms);
   if (f32)
-    return to_status(T ? mns::launch_full_kk_f32(*P, max_k, grid, st)
-                       : mns::launch_full_kmn_f32(*P, max_k, grid, st));
-  return to_status(T ? mns::launch_full_kk(*P, max_k, grid, st)
-                     : mns::launch_full_kmn(*P, max_k, grid, st));
+    return to_status(T ? mns::launch_full_kk_f32(*P, mode, max_k, grid, st)
+                       : mns::launch_full_kmn_f32(*P, mode, max_k, grid, st));
+  return to_status(T ? mns::launch_full_kk(*P, mode, max_k, grid, st)
+                     : mns::launch_full_kmn(*P, mode, max_k, grid, st));
 }
 
 int run_normalize(const Problem& p, const Layout& L, const void* G, void* X, float eps,
