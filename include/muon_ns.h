@@ -199,6 +199,42 @@ int muon_ns_grouped_workspace_size(const muon_ns_stack* stacks, int num_stacks, 
 int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, const float* coeffs,
                     float eps, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Stacks held in host memory (e.g. optimizer states kept on the CPU).  The
+ * stack is processed in chunks of `chunk` matrices: each chunk is uploaded,
+ * orthogonalised and downloaded, and the copies of one chunk overlap the
+ * compute of its neighbours (two chunks in flight; uploads and downloads run
+ * on two streams the library creates once per device, the compute on
+ * `stream`).  The matrices of a stack are independent (the leading axis is
+ * the batch, prime-rl PR #3873, Summary item 2), so the result equals
+ * muon_ns_ws() on the whole stack bit for bit.  Host buffers should be
+ * page-locked (cudaHostAlloc, or a pinned torch tensor) for the copies to
+ * overlap; pageable memory gives the same result without overlap.
+ * ------------------------------------------------------------------------- */
+
+/* Device workspace bytes for muon_ns_host(): the call's error word (256
+ * bytes, then padding to 1 KB) and two slots of (input chunk, output chunk,
+ * muon_ns_ws() workspace of one chunk).  chunk <= 0 selects the default,
+ * ceil(batch / 8); chunk > batch is clamped to batch.  Returns MUON_NS_OK or
+ * MUON_NS_ERR_INVALID_ARG / MUON_NS_ERR_ALIGNMENT as muon_ns_workspace_size(). */
+int muon_ns_host_workspace_size(int batch, int rows, int cols, int chunk, size_t* bytes);
+
+/* out_host = NS(G_host).
+ *   G_host, out_host  host, bf16 [batch][rows][cols]; they may be the same
+ *                     buffer, otherwise they must not overlap;
+ *   chunk             matrices per chunk (<= 0: the default above);
+ *   workspace         device, >= muon_ns_host_workspace_size() bytes,
+ *                     256-byte aligned, caller-owned.
+ * Everything is enqueued and the call returns: `stream` completes after the
+ * last download, so synchronise it before reading out_host.  The device
+ * error word is the workspace's first int (muon_ns_read_error()).  Kernel
+ * launches: 1 + 3 * steps per chunk; one cudaMemcpyAsync per chunk and
+ * direction.  Errors as muon_ns_ws(); MUON_NS_ERR_CUDA if a copy, stream or
+ * event operation fails. */
+int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int rows, int cols,
+                 int steps, const float* coeffs, float eps, int chunk, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, copies the device error word of `workspace` into
  * *device_error (0 = none) and, if `clear` is nonzero, resets it.  Returns
  * MUON_NS_ERR_TIMEOUT if the word is nonzero, else MUON_NS_OK or an error. */

@@ -16,6 +16,8 @@ from .ns import (  # noqa: F401
     muon_ns_gram,
     muon_ns_grouped,
     grouped_workspace_size,
+    host_workspace_size,
+    muon_ns_host,
     muon_ns_normalize,
     muon_ns_normalize_static,
     muon_ns_poly,

@@ -772,6 +772,162 @@ int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, cons
   return run_ns_stacks(S, ns, steps, abc, eps, err, d.sms, stream);
 }
 
+// ------------------------------------------------------- host-held stacks --
+
+}  // extern "C"
+
+namespace {
+
+// Streams and events of the host-buffer path, created once per device: one
+// stream for uploads, one for downloads; per slot, the events "input
+// uploaded", "chunk computed" and "output downloaded".
+struct HostPipe {
+  bool ready;
+  cudaStream_t up, down;
+  cudaEvent_t start, in[2], done[2], out[2];
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+int host_pipe_init(HostPipe* hp) {
+  if (hp->ready) return MUON_NS_OK;
+  if (cudaStreamCreateWithFlags(&hp->up, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hp->down, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  for (int i = 0; i < 2; ++i)
+    if (cudaEventCreateWithFlags(&hp->in[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp->done[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp->out[i], cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return MUON_NS_ERR_CUDA;
+    }
+  hp->ready = true;
+  return MUON_NS_OK;
+}
+
+inline int host_chunk(int batch, int chunk) {
+  if (chunk > 0) return chunk < batch ? chunk : batch;
+  const int c = (batch + 7) / 8;
+  return c < 1 ? 1 : c;
+}
+
+// Host-path workspace: the call's error word, then two slots of (input
+// chunk, output chunk, NS workspace for one chunk).
+struct HostLayout {
+  size_t in, out, ws, slot, total;
+};
+
+HostLayout host_layout(const Problem& pc) {
+  HostLayout H;
+  const size_t chunk_bytes = 2 * static_cast<size_t>(pc.batch) * pc.R * pc.C;
+  H.in = 0;
+  H.out = round_up(chunk_bytes, 1024);
+  H.ws = H.out + round_up(chunk_bytes, 1024);
+  H.slot = round_up(H.ws + make_layout(pc).total, 1024);
+  H.total = 1024 + 2 * H.slot;
+  return H;
+}
+
+}  // namespace
+
+extern "C" {
+
+int muon_ns_host_workspace_size(int batch, int rows, int cols, int chunk, size_t* bytes) {
+  if (!bytes) return MUON_NS_ERR_INVALID_ARG;
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (empty) {
+    *bytes = 0;
+    return MUON_NS_OK;
+  }
+  Problem pc;
+  check_shape(host_chunk(batch, chunk), rows, cols, &pc, &empty);
+  *bytes = host_layout(pc).total;
+  return MUON_NS_OK;
+}
+
+int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int rows, int cols,
+                 int steps, const float* coeffs, float eps, int chunk, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  float abc[3];
+  if ((s = check_scalars(steps, coeffs, eps, abc)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!G_host || !out_host) return MUON_NS_ERR_INVALID_ARG;
+  const int cb = host_chunk(batch, chunk);
+  Problem pc;
+  check_shape(cb, rows, cols, &pc, &empty);
+  const HostLayout H = host_layout(pc);
+  if (!workspace || workspace_bytes < H.total) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  int dev = 0;
+  if ((s = current_device_info(&d, &dev)) != MUON_NS_OK) return s;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe& hp = g_pipe[dev];
+  if ((s = host_pipe_init(&hp)) != MUON_NS_OK) return s;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(base);
+  const size_t mat = static_cast<size_t>(rows) * cols;
+  const int nchunks = (batch + cb - 1) / cb;
+  auto fail = [] {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  };
+  // The copy streams start after all work already queued on `stream` (so a
+  // workspace reused from a previous call is free) and the error word is clear.
+  if (cudaMemsetAsync(base, 0, 256, stream) != cudaSuccess ||
+      cudaEventRecord(hp.start, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(hp.up, hp.start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp.down, hp.start, 0) != cudaSuccess)
+    return fail();
+  for (int i = 0; i < nchunks; ++i) {
+    const int sl = i & 1;
+    const long long b0 = static_cast<long long>(i) * cb;
+    const int nb = static_cast<int>(batch - b0 < cb ? batch - b0 : cb);
+    const size_t bytes = 2 * mat * nb;
+    uint8_t* slot = base + 1024 + sl * H.slot;
+    uint16_t* din = reinterpret_cast<uint16_t*>(slot + H.in);
+    uint16_t* dout = reinterpret_cast<uint16_t*>(slot + H.out);
+    // Upload once chunk i - 2 has finished reading this slot's input.
+    if (i >= 2 && cudaStreamWaitEvent(hp.up, hp.done[sl], 0) != cudaSuccess) return fail();
+    if (cudaMemcpyAsync(din, G_host + b0 * mat, bytes, cudaMemcpyHostToDevice, hp.up) != cudaSuccess ||
+        cudaEventRecord(hp.in[sl], hp.up) != cudaSuccess)
+      return fail();
+    // Compute once the input is up and chunk i - 2's output has been downloaded.
+    if (cudaStreamWaitEvent(stream, hp.in[sl], 0) != cudaSuccess) return fail();
+    if (i >= 2 && cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
+    Problem pi;
+    check_shape(nb, rows, cols, &pi, &empty);
+    Stack S;
+    S.p = pi;
+    S.L = make_layout(pi);
+    S.G = din;
+    S.out = dout;
+    S.ws = slot + H.ws;
+    S.cur = nullptr;
+    if ((s = run_ns_stacks(&S, 1, steps, abc, eps, err, d.sms, stream)) != MUON_NS_OK) return s;
+    if (cudaEventRecord(hp.done[sl], stream) != cudaSuccess) return fail();
+    // Download once computed.
+    if (cudaStreamWaitEvent(hp.down, hp.done[sl], 0) != cudaSuccess ||
+        cudaMemcpyAsync(out_host + b0 * mat, dout, bytes, cudaMemcpyDeviceToHost, hp.down) != cudaSuccess ||
+        cudaEventRecord(hp.out[sl], hp.down) != cudaSuccess)
+      return fail();
+  }
+  // `stream` completes after the last downloads.
+  for (int sl = 0; sl < 2 && sl < nchunks; ++sl)
+    if (cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
+  return MUON_NS_OK;
+}
+
 int muon_ns_read_error(const void* workspace, int* device_error, int clear, cudaStream_t stream) {
   if (!workspace || !device_error) return MUON_NS_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) {

@@ -255,3 +255,38 @@ def muon_ns_f32(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: flo
         _lib.check(_lib.lib().muon_ns_ws_f32(_ptr(G), _ptr(out), b, r, c, int(steps), _coeffs(coeffs), float(eps),
                                              _ptr(workspace), workspace.numel(), _stream(G.device)), "muon_ns_ws_f32")
     return out
+
+
+def host_workspace_size(batch: int, rows: int, cols: int, chunk: int = 0) -> int:
+    """Device workspace bytes muon_ns_host needs (chunk <= 0: the default)."""
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_ns_host_workspace_size(int(batch), int(rows), int(cols), int(chunk), ctypes.byref(n)),
+               "muon_ns_host_workspace_size")
+    return n.value
+
+
+def muon_ns_host(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS,
+                 out: torch.Tensor | None = None, chunk: int = 0, workspace: torch.Tensor | None = None,
+                 device=None, sync: bool = True) -> torch.Tensor:
+    """NS of a bf16 matrix or stack held in host memory: the library uploads,
+    orthogonalises and downloads it in chunks of `chunk` matrices, the copies
+    overlapping the compute.  `out` (host, may be G) receives the result;
+    with sync=False the caller synchronises the current stream of `device`
+    before reading it.  Pin G and out (Tensor.pin_memory()) for overlap."""
+    if not isinstance(G, torch.Tensor) or G.dtype != torch.bfloat16 or G.is_cuda or not G.is_contiguous():
+        raise TypeError("G must be a contiguous host bfloat16 tensor")
+    b, r, c = _shape3(G)
+    if out is None:
+        out = torch.empty_like(G, pin_memory=G.is_pinned())
+    if out.dtype != torch.bfloat16 or out.is_cuda or out.shape != G.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous host bfloat16 tensor shaped like G")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if workspace is None:
+        workspace = torch.empty(max(host_workspace_size(b, r, c, chunk), 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.lib().muon_ns_host(_ptr(G), _ptr(out), b, r, c, int(steps), _coeffs(coeffs), float(eps),
+                                           int(chunk), _ptr(workspace), workspace.numel(), _stream(dev)),
+                   "muon_ns_host")
+        if sync:
+            torch.cuda.current_stream(dev).synchronize()
+    return out

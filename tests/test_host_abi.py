@@ -316,3 +316,47 @@ def test_f32_workspace_regions_hold_fp32():
     p = ctypes.c_void_p(4096)
     assert L.muon_ns_ws_f32(p, p, 1, 12, 16, 5, None, 1e-7, p, 1 << 30, None) == _lib.ERR_ALIGNMENT
     assert L.muon_ns_ws_f32(p, p, 1, 16, 16, 5, None, 1e-7, p, 16, None) == _lib.ERR_WORKSPACE
+
+
+# ---------------------------------------------------------- host-held stacks --
+
+def _call_host(**kw):
+    L = _lib.lib()
+    args = dict(G=4096, out=4096, batch=16, rows=64, cols=128, steps=5, eps=1e-7, chunk=0,
+                ws=4096, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return L.muon_ns_host(ctypes.c_void_p(args["G"]), ctypes.c_void_p(args["out"]), args["batch"], args["rows"],
+                          args["cols"], args["steps"], None, args["eps"], args["chunk"], ctypes.c_void_p(args["ws"]),
+                          args["wsb"], args["stream"])
+
+
+def test_host_path_workspace_arithmetic():
+    def ws(b, r, c, chunk=0):
+        return ns.host_workspace_size(b, r, c, chunk)
+    one = ns.workspace_size(1, 256, 512)
+    # error word + 2 slots of (input chunk, output chunk, NS workspace of a chunk)
+    for chunk in (1, 3, 16):
+        slot = 2 * chunk * 256 * 512 * 2 + ns.workspace_size(chunk, 256, 512)
+        assert 2 * slot <= ws(16, 256, 512, chunk) <= 2 * slot + 1024 + 4 * 1024
+    assert ws(16, 256, 512) == ws(16, 256, 512, 2)      # default chunk ceil(16 / 8) = 2
+    assert ws(17, 256, 512) == ws(17, 256, 512, 3)      # ceil(17 / 8) = 3
+    assert ws(4, 256, 512, 100) == ws(4, 256, 512, 4)   # clamped to the batch
+    assert ws(16, 256, 512, 4) > ws(16, 256, 512, 2) > one
+    assert ws(0, 256, 512) == 0
+
+
+def test_host_path_argument_errors():
+    assert _call_host(G=0) == _lib.ERR_INVALID_ARG
+    assert _call_host(out=0) == _lib.ERR_INVALID_ARG
+    assert _call_host(rows=60) == _lib.ERR_ALIGNMENT
+    assert _call_host(steps=-1) == _lib.ERR_INVALID_ARG
+    assert _call_host(batch=-1) == _lib.ERR_INVALID_ARG
+    assert _call_host(wsb=1024) == _lib.ERR_WORKSPACE
+    assert _call_host(ws=0) == _lib.ERR_WORKSPACE
+    assert _call_host(ws=4096 + 16) == _lib.ERR_ALIGNMENT
+    assert _call_host(batch=0) == _lib.OK  # empty stack: nothing to do
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_host_path_without_device_is_unsupported():
+    assert _call_host() == _lib.ERR_UNSUPPORTED_DEVICE
