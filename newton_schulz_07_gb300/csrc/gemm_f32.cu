@@ -23,7 +23,7 @@ cudaError_t launch_sym_mnmn_f32(const GemmParams& p, PairMode mode, int grid, cu
 template <bool B_MN>
 cudaError_t launch_full_f32(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream) {
   if (mode == kPairMma) return launch_tc_gemm<false, B_MN, false, 4, true, 2, true>(p, grid, stream);
-  return max_k <= 1024 ? launch_tc_gemm<false, B_MN, false, 8, true, 1, false>(p, grid, stream)
+  return max_k <= kShortK ? launch_tc_gemm<false, B_MN, false, 8, true, 1, false>(p, grid, stream)
                        : launch_tc_gemm<false, B_MN, false, 4, true, 1, false>(p, grid, stream);
 }
 

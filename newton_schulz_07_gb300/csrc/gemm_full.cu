@@ -11,7 +11,7 @@ template <bool B_MN>
 cudaError_t launch_full(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream) {
   if (mode == kSingle) return cudaErrorInvalidValue;
   if (mode == kPairMma) return launch_tc_gemm<false, B_MN, false, 4, false, 2, true>(p, grid, stream);
-  return max_k <= 1024 ? launch_tc_gemm<false, B_MN, false, 8, false, 2, false>(p, grid, stream)
+  return max_k <= kShortK ? launch_tc_gemm<false, B_MN, false, 8, false, 2, false>(p, grid, stream)
                        : launch_tc_gemm<false, B_MN, false, 4, false, 2, false>(p, grid, stream);
 }
 

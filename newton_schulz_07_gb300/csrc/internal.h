@@ -30,8 +30,9 @@ enum PairMode : int {
 #ifndef MNS_PAIR_MMA
 #define MNS_PAIR_MMA 1
 #endif
+constexpr int kShortK = 1024;  // contractions up to this are "short"
 inline PairMode pair_mode(bool f32, int max_k) {
-  if (MNS_PAIR_MMA && max_k > 1024) return kPairMma;
+  if (MNS_PAIR_MMA && max_k > kShortK) return kPairMma;
   return f32 ? kSingle : kMulticast;
 }
 

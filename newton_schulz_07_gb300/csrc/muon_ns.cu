@@ -425,9 +425,33 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
           members[ng++] = i;
         }
         if (ng == 0) continue;
-        if ((s = run_gram(io, ng, eps, err, sms, st)) != MUON_NS_OK) return s;
-        if ((s = run_poly(io, ng, abc[1], abc[2], err, sms, st)) != MUON_NS_OK) return s;
-        if ((s = run_update(io, ng, abc[0], eps, k + 1 < steps, err, sms, st)) != MUON_NS_OK)
+        // Each product runs as one launch per contraction regime: stacks with
+        // short contractions (K <= kShortK) and long ones take different pair
+        // modes and epilogues, and sharing a launch would give one of them
+        // the other's.
+        StepIO sub[mns::kMaxGroups];
+        auto split = [&](auto run, auto contraction) {
+          for (int longk = 0; longk < 2; ++longk) {
+            int n = 0;
+            for (int j = 0; j < ng; ++j)
+              if ((contraction(io[j].p) > mns::kShortK) == (longk != 0)) sub[n++] = io[j];
+            if (n == 0) continue;
+            const int r = run(sub, n);
+            if (r != MUON_NS_OK) return r;
+          }
+          return static_cast<int>(MUON_NS_OK);
+        };
+        auto K_n = [](const Problem& q) { return q.n; };
+        auto K_m = [](const Problem& q) { return q.m; };
+        if ((s = split([&](const StepIO* v, int n) { return run_gram(v, n, eps, err, sms, st); }, K_n)) !=
+            MUON_NS_OK)
+          return s;
+        if ((s = split([&](const StepIO* v, int n) { return run_poly(v, n, abc[1], abc[2], err, sms, st); },
+                       K_m)) != MUON_NS_OK)
+          return s;
+        if ((s = split([&](const StepIO* v, int n) {
+               return run_update(v, n, abc[0], eps, k + 1 < steps, err, sms, st);
+             }, K_m)) != MUON_NS_OK)
           return s;
         for (int j = 0; j < ng; ++j) S[members[j]].cur = io[j].Xn;
       }
