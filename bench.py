@@ -527,29 +527,44 @@ def time_grouped(torch, ns, wls, dev, peaks, steps=10, warmup=3):
     outs = [torch.empty_like(G) for G in Gs]
     ws = torch.empty(ns.grouped_workspace_size(Gs), dtype=torch.uint8, device=dev)
     scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
+    sws = [ns.alloc_workspace(*G.shape, device=dev) for G in Gs]
+
+    def grouped():
         ns.muon_ns_grouped(Gs, outs=outs, workspace=ws)
-    torch.cuda.synchronize()
+
+    def separate():  # the same stacks as back-to-back muon_ns_ws calls
+        for G, o, w in zip(Gs, outs, sws):
+            ns.muon_ns(G, out=o, workspace=w)
+
     stream = torch.cuda.current_stream(dev)
-    tot = 0.0
-    for i in range(steps):
-        scrub.fill_(i & 0xFF)
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        ns.muon_ns_grouped(Gs, outs=outs, workspace=ws)
-        e.record(stream)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
         torch.cuda.synchronize()
-        tot += s.elapsed_time(e)
-    ms = tot / steps
+        tot = 0.0
+        for i in range(steps):
+            scrub.fill_(i & 0xFF)
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            tot += s.elapsed_time(e)
+        return tot / steps
+
+    sep_ms = timed(separate)
+    ms = timed(grouped)
     dense = sum(w.dense_flops() for w in wls)
     tf = dense / (ms * 1e-3) / 1e12
     res = {"ms": ms, "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
            "stacks": [w.name for w in wls], "api": "muon_ns_grouped (one call)", "steps": steps,
+           "separate_calls_ms": sep_ms,
            "l2": "flushed between timed steps", "device_error_word": ns.read_error(ws)}
     if all(w.name in PAGES_H200_QUACK_MS for w in wls):
         res["pages_h200_quack_ms_sum"] = sum(PAGES_H200_QUACK_MS[w.name] for w in wls)
-    del Gs, outs, ws, scrub
+    del Gs, outs, ws, sws, scrub
     torch.cuda.empty_cache()
     return res
 
