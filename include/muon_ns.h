@@ -214,15 +214,19 @@ int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, cons
 
 /* Device workspace bytes for muon_ns_host(): the call's error word (256
  * bytes, then padding to 1 KB) and two slots of (input chunk, output chunk,
- * muon_ns_ws() workspace of one chunk).  chunk <= 0 selects the default,
- * ceil(batch / 8); chunk > batch is clamped to batch.  Returns MUON_NS_OK or
- * MUON_NS_ERR_INVALID_ARG / MUON_NS_ERR_ALIGNMENT as muon_ns_workspace_size(). */
+ * muon_ns_ws() workspace of one chunk of `chunk` matrices).  `chunk` is the
+ * largest chunk: when the stack is larger, the first and the last chunk take
+ * ceil(chunk / 2) matrices (shorter upload before the first compute and
+ * download after the last) and the ones between `chunk`, the one before the
+ * last the remainder.  chunk <= 0 selects ceil(batch / 4); chunk > batch is
+ * clamped to batch.  Returns MUON_NS_OK or MUON_NS_ERR_INVALID_ARG /
+ * MUON_NS_ERR_ALIGNMENT as muon_ns_workspace_size(). */
 int muon_ns_host_workspace_size(int batch, int rows, int cols, int chunk, size_t* bytes);
 
 /* out_host = NS(G_host).
  *   G_host, out_host  host, bf16 [batch][rows][cols]; they may be the same
  *                     buffer, otherwise they must not overlap;
- *   chunk             matrices per chunk (<= 0: the default above);
+ *   chunk             largest chunk, as above (<= 0: the default);
  *   workspace         device, >= muon_ns_host_workspace_size() bytes,
  *                     256-byte aligned, caller-owned.
  * Everything is enqueued and the call returns: `stream` completes after the

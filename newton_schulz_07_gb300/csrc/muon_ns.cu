@@ -832,10 +832,28 @@ int host_pipe_init(HostPipe* hp) {
   return MUON_NS_OK;
 }
 
+// Largest chunk of a host-path call.  Default ceil(batch / 4): with the
+// half-size first and last chunks below, four full chunks keep each NS call
+// large (few partial waves) while the first upload and the last download,
+// which nothing overlaps, stay at an eighth of the stack each.
 inline int host_chunk(int batch, int chunk) {
   if (chunk > 0) return chunk < batch ? chunk : batch;
-  const int c = (batch + 7) / 8;
+  const int c = (batch + 3) / 4;
   return c < 1 ? 1 : c;
+}
+
+// Size of chunk i of a host-path call with largest chunk c: the first and
+// (when the stack spans more than one chunk) the last take ceil(c / 2)
+// matrices, the ones in between c, the one before the last the remainder.
+// Returns 0 past the end.
+inline int host_chunk_size(int batch, int c, int i) {
+  if (batch <= c) return i == 0 ? batch : 0;
+  const int h = (c + 1) / 2;
+  const int mid = batch - 2 * h;  // matrices between the half-size ends (>= 0 since c < batch)
+  const int nmid = (mid + c - 1) / c;
+  if (i == 0) return h;
+  if (i <= nmid) return (i < nmid) ? c : mid - (nmid - 1) * c;
+  return i == nmid + 1 ? h : 0;
 }
 
 // Host-path workspace: the call's error word, then two slots of (input
@@ -901,7 +919,6 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
   uint8_t* base = static_cast<uint8_t*>(workspace);
   int* err = reinterpret_cast<int*>(base);
   const size_t mat = static_cast<size_t>(rows) * cols;
-  const int nchunks = (batch + cb - 1) / cb;
   auto fail = [] {
     cudaGetLastError();
     return MUON_NS_ERR_CUDA;
@@ -913,10 +930,13 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
       cudaStreamWaitEvent(hp.up, hp.start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp.down, hp.start, 0) != cudaSuccess)
     return fail();
-  for (int i = 0; i < nchunks; ++i) {
+  long long b0 = 0;
+  int nchunks = 0;
+  for (int i = 0;; ++i) {
+    const int nb = host_chunk_size(batch, cb, i);
+    if (nb == 0) break;
+    nchunks = i + 1;
     const int sl = i & 1;
-    const long long b0 = static_cast<long long>(i) * cb;
-    const int nb = static_cast<int>(batch - b0 < cb ? batch - b0 : cb);
     const size_t bytes = 2 * mat * nb;
     uint8_t* slot = base + 1024 + sl * H.slot;
     uint16_t* din = reinterpret_cast<uint16_t*>(slot + H.in);
@@ -945,6 +965,7 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
         cudaMemcpyAsync(out_host + b0 * mat, dout, bytes, cudaMemcpyDeviceToHost, hp.down) != cudaSuccess ||
         cudaEventRecord(hp.out[sl], hp.down) != cudaSuccess)
       return fail();
+    b0 += nb;
   }
   // `stream` completes after the last downloads.
   for (int sl = 0; sl < 2 && sl < nchunks; ++sl)

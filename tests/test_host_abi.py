@@ -338,8 +338,8 @@ def test_host_path_workspace_arithmetic():
     for chunk in (1, 3, 16):
         slot = 2 * chunk * 256 * 512 * 2 + ns.workspace_size(chunk, 256, 512)
         assert 2 * slot <= ws(16, 256, 512, chunk) <= 2 * slot + 1024 + 4 * 1024
-    assert ws(16, 256, 512) == ws(16, 256, 512, 2)      # default chunk ceil(16 / 8) = 2
-    assert ws(17, 256, 512) == ws(17, 256, 512, 3)      # ceil(17 / 8) = 3
+    assert ws(16, 256, 512) == ws(16, 256, 512, 4)      # default largest chunk ceil(16 / 4) = 4
+    assert ws(17, 256, 512) == ws(17, 256, 512, 5)      # ceil(17 / 4) = 5
     assert ws(4, 256, 512, 100) == ws(4, 256, 512, 4)   # clamped to the batch
     assert ws(16, 256, 512, 4) > ws(16, 256, 512, 2) > one
     assert ws(0, 256, 512) == 0
