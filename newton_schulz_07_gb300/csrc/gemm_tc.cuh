@@ -2,9 +2,11 @@
 //
 //   out[i, j] = alpha * sum_k Aop[i, k] * Bop[k, j] + beta * addend[i, j]
 //
-// bf16 operands staged by TMA into 128-byte-swizzled shared memory, fp32
-// accumulation in TMEM by tcgen05.mma (M = 128, N = 256, K = 16 per
-// instruction), fp32 epilogue, one rounding to bf16.
+// bf16 operands (or fp32 operands read as tf32, F32) staged by TMA into
+// 128-byte-swizzled shared memory, fp32 accumulation in TMEM by tcgen05.mma
+// (M = 128, or 256 across a CTA pair with SM2; N = 256; K = 16 per
+// instruction, 8 for tf32), fp32 epilogue, one rounding of the output (to
+// bf16, or to tf32 in fp32 storage where it feeds another product).
 //
 // With the optional fp32 diagonal (GroupArgs::diag_out / diag_in) the
 // polynomial product stores B = D + O as an fp32 vector D = diag(B) and a bf16
@@ -41,7 +43,8 @@
 //
 // Roles (64 + 32 * kEpiWarps threads, one CTA per SM, persistent):
 //   warp 0 lane 0   TMA producer: fills a kStages-deep ring of operand stages
-//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma per stage into one of two
+//   warp 1 lane 0   MMA issuer (with SM2 in CTA 0 of the pair only):
+//                   tcgen05.mma per K slice of a stage into one of two
 //                   256-column TMEM accumulators, commits release the stage
 //   warps 2..       epilogue: each warp reads its 32-lane TMEM quarter for its
 //                   share of the columns (two warps per quarter by default),
