@@ -33,7 +33,8 @@
  *
  * Conventions for every entry point below:
  *   - Matrices are contiguous row-major stacks [batch][rows][cols] of raw
- *     bf16 bit patterns (muon_bf16) in DEVICE memory owned by the caller.
+ *     bf16 bit patterns (muon_bf16) in DEVICE memory owned by the caller
+ *     (muon_ns_host() alone takes its stacks in host memory).
  *   - rows and cols must be multiples of 8 and every device pointer must be
  *     16-byte aligned (16-byte rows for TMA; prime-rl PR #3873, Summary
  *     item 1, has the same divisible-by-8 rule).  This is an
