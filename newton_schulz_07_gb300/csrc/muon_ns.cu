@@ -1,15 +1,23 @@
 // C-ABI entry points (include/muon_ns.h): argument checks, workspace layout,
 // TMA tensor maps and the launch sequence of one batched NS call.
 //
-//   norm (ns_norm_partial) -> scale (ns_scale) -> steps x [Gram, poly, update]
+//   norm (ns_norm_partial) -> steps x [Gram, poly, update]
 //
-// Tall inputs (rows > cols) are never transposed in memory: with Y = X^T kept
-// in the input's orientation, A = Y^T Y reads Y MN-major, and the update
-// Y' = a Y + Y B reads B K-major (B is bit-symmetric), so the result lands in
-// the input orientation directly.
+// The first step reads G itself and applies s = 1 / (||G||_F + eps) in its
+// epilogues, so no scaled copy of G is made; steps == 0 runs the norm and the
+// scale kernel (ns_scale) instead.  Each product launch takes one pair mode
+// from its longest contraction (pair_mode in internal.h), and builds its tile
+// space and B-operand boxes from it.
+//
+// Tall inputs (rows > cols) are never transposed in memory (bf16): with
+// Y = X^T kept in the input's orientation, A = Y^T Y reads Y MN-major, and the
+// update Y' = a Y + Y B reads B K-major (B is bit-symmetric), so the result
+// lands in the input orientation directly.  The fp32 mode keeps every operand
+// K-major and holds the iterate in both orientations instead.
 //
 // The iterate ping-pongs between the workspace and `out`, starting where the
-// parity of `steps` makes the last step write `out`; there is no final copy.
+// parity of `steps` makes the last step write `out`; only in place
+// (out == G) with an odd step count is the result copied once at the end.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
