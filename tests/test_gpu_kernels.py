@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 KERNEL_TOL = 3e-3
 
 SHAPES = [(1, 8, 8), (3, 136, 264), (2, 256, 512), (2, 264, 136), (1, 392, 200), (1, 200, 392),
-          (2, 128, 128), (1, 520, 1040), (1, 1040, 520), (1, 1096, 1304), (1, 1304, 1096)]
+          (2, 128, 128), (1, 520, 1040), (1, 1040, 520), (1, 1096, 1304), (1, 1304, 1096),
+          (1, 1024, 1032), (1, 1032, 1024)]  # contraction 1024 (multicast pairs) next to 1032 (2-SM MMAs)
 
 
 def f64(bits):
@@ -64,7 +65,8 @@ def test_gram(shape):
     assert max(per_matrix_rel(f64(a), ref)) <= KERNEL_TOL
 
 
-@pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1040), (2, 1096)])
+@pytest.mark.parametrize("batch,m", [(1, 8), (2, 136), (3, 256), (1, 392), (2, 520), (1, 1024), (1, 1032), (1, 1040),
+                                     (2, 1096)])
 @pytest.mark.parametrize("split_diag", [False, True])
 def test_poly(batch, m, split_diag):
     bits = symmetric_bits(batch, m, seed=m)
