@@ -24,9 +24,12 @@
  * accumulates in fp32 on the tensor cores and every epilogue (b·A + c·(A A),
  * a·X + B X) runs in fp32 and rounds once to bf16, as the fp32 alpha/beta
  * epilogue of prime-rl PR #3873 (Results, note under the microbenchmark).
- * A and B are stored bit-symmetric: one triangle is computed and mirrored
- * (prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381 "Add
- * --muon-use-syrk option", Summary).  The diagonal of B is kept in fp32
+ * A and B are symmetric and one triangle of each is computed (prime-rl PR
+ * #3873, Summary item 1; Megatron-LM PR #6381 "Add --muon-use-syrk option",
+ * Summary).  The per-step entry points mirror it, so the stored matrix is
+ * bit-symmetric; the whole-call entry points mirror it only inside the
+ * diagonal 256 x 256 blocks and the next product reads the rest of the upper
+ * triangle transposed from the lower one.  The diagonal of B is kept in fp32
  * (B = D + O, O bf16 with a zero diagonal) and the update applies (a + D)
  * in its fp32 epilogue: the same arithmetic, with the part of B that
  * dominates near convergence kept out of bf16 rounding.
@@ -101,8 +104,11 @@ enum {
   MUON_NS_WS_ERROR = 1,   /* int32 device error word */
   MUON_NS_WS_NORMS = 2,   /* fp32 [batch]: ||G_k||_F of the last call */
   MUON_NS_WS_X = 3,       /* bf16 [batch][rows][cols]: ping-pong iterate */
-  MUON_NS_WS_GRAM = 4,    /* bf16 [batch][m][m]: A of the last step, m = min(rows, cols) */
-  MUON_NS_WS_POLY = 5,    /* bf16 [batch][m][m]: off-diagonal part of B of the last step */
+  MUON_NS_WS_GRAM = 4,    /* bf16 [batch][m][m]: A of the last step, m = min(rows, cols); the
+                             whole-call entry points store its lower triangle and its diagonal
+                             256 x 256 blocks only (the products read the rest transposed) */
+  MUON_NS_WS_POLY = 5,    /* bf16 [batch][m][m]: off-diagonal part of B of the last step, stored
+                             like A */
   MUON_NS_WS_DIAG = 6     /* fp32 [batch][m]: diagonal of B of the last step */
 };
 
@@ -111,8 +117,8 @@ enum {
 int muon_ns_workspace_size(int batch, int rows, int cols, size_t* bytes);
 
 /* Offset and size in bytes of one region of the workspace (layout above).
- * Tests read A (MUON_NS_WS_GRAM) after a call with steps = 1 to check that it
- * is bit-symmetric. */
+ * Tests read A (MUON_NS_WS_GRAM) after a call with steps = 1 to check its
+ * stored part against the definition. */
 int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* offset, size_t* bytes);
 
 /* out = NS(G) for a stack of `batch` matrices of rows x cols.

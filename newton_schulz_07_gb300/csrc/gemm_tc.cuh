@@ -186,6 +186,10 @@ struct GroupArgs {
   //   SYM (Gram)      out = alpha s^2 acc
   //   FULL (update)   out = alpha s acc + (beta + diag) s addend
   const float* norms;
+  // Operands read from a half-stored symmetric matrix (GemmParams::half_out
+  // of the product that wrote it): k-blocks past the operand rows' diagonal
+  // 256-block are read transposed, MN-major, through tmA2 / tmB2.
+  int half_a, half_b;
 };
 
 struct GemmParams {
@@ -196,6 +200,8 @@ struct GemmParams {
   // written when out_t != 0.  The fp32 path keeps its iterate in both
   // orientations so that every tensor-core operand is K-major.
   CUtensorMap tmOutT[kMaxGroups];
+  CUtensorMap tmA2[kMaxGroups];   // MN-major maps of half-stored operands
+  CUtensorMap tmB2[kMaxGroups];
   GroupArgs grp[kMaxGroups];
   int num_groups;
   long long total_tiles;
@@ -203,6 +209,10 @@ struct GemmParams {
   int diag_per_col;
   int round_tf32;     // F32 only: store outputs rounded to tf32 (they feed an MMA)
   int out_t;          // FULL only: also write the transposed output through tmOutT
+  // SYM only: half storage.  A value is mirrored only inside its diagonal
+  // 256 x 256 block; elsewhere only the lower triangle is written, and
+  // consumers read the upper part from it transposed (GroupArgs::half_a/b).
+  int half_out;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -393,26 +403,32 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           const uint32_t sb = sa + kABytes;
           const int k0 = kb * EC::kBlockK;
           constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
+          // Operands of a half-stored matrix: past the rows' diagonal 256-block
+          // the k-block is read transposed (MN-major) from the lower triangle.
+          const bool amn = A_MN || (G.half_a && k0 >= 256 * ((I >> 1) + 1));
+          const bool bmn = B_MN || (G.half_b && k0 >= 256 * (J + 1));
+          const CUtensorMap* mA = (amn && !A_MN) ? &P.tmA2[gr] : tmA;
+          const CUtensorMap* mB = (bmn && !B_MN) ? &P.tmB2[gr] : tmB;
           if (SM2) {
             // This CTA's A tile and its half of the B panel, into its own
             // shared memory; all bytes of the pair are counted on CTA 0's
             // barrier, which expects both CTAs' stages.
             const uint32_t fb = ptx::mapa(sy.full(stage), 0);
             if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), 2 * R::kStageBytes);
-            if (A_MN) {
+            if (amn) {
 #pragma unroll
               for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
-                ptx::tma_load_3d_pair(sa + c * EC::kMnChunkBytes, tmA, fb, row0 + c * EC::kMnChunk, k0, b);
+                ptx::tma_load_3d_pair(sa + c * EC::kMnChunkBytes, mA, fb, row0 + c * EC::kMnChunk, k0, b);
             } else {
-              ptx::tma_load_3d_pair(sa, tmA, fb, k0, row0, b);
+              ptx::tma_load_3d_pair(sa, mA, fb, k0, row0, b);
             }
-            if (B_MN) {
+            if (bmn) {
 #pragma unroll
               for (int c = 0; c < kNch / 2; ++c)
-                ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, tmB, fb,
+                ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, mB, fb,
                                       col0 + (static_cast<int>(crank) * (kNch / 2) + c) * EC::kMnChunk, k0, b);
             } else {
-              ptx::tma_load_3d_pair(sb, tmB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
+              ptx::tma_load_3d_pair(sb, mB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
             }
             issued_mask |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -423,34 +439,34 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             continue;
           }
           ptx::mbar_arrive_expect_tx(sy.full(stage), R::kStageBytes);
-          if (A_MN) {
+          if (amn) {
 #pragma unroll
             for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
-              ptx::tma_load_3d(sa + c * EC::kMnChunkBytes, tmA, sy.full(stage),
+              ptx::tma_load_3d(sa + c * EC::kMnChunkBytes, mA, sy.full(stage),
                                row0 + c * EC::kMnChunk, k0, b);
           } else {
-            ptx::tma_load_3d(sa, tmA, sy.full(stage), k0, row0, b);
+            ptx::tma_load_3d(sa, mA, sy.full(stage), k0, row0, b);
           }
           if (CL == 2) {
             // This CTA's half of the shared panel, into both CTAs.
-            if (B_MN) {
+            if (bmn) {
 #pragma unroll
               for (int c = 0; c < kNch / 2; ++c) {
                 const int cg = static_cast<int>(crank) * (kNch / 2) + c;
-                ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, tmB, sy.full(stage),
+                ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, mB, sy.full(stage),
                                     col0 + cg * EC::kMnChunk, k0, b, 0x3);
               }
             } else {
-              ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), tmB, sy.full(stage), k0,
+              ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), mB, sy.full(stage), k0,
                                   col0 + static_cast<int>(crank) * (kTileN / 2), b, 0x3);
             }
-          } else if (B_MN) {
+          } else if (bmn) {
 #pragma unroll
             for (int c = 0; c < kNch; ++c)
-              ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, tmB, sy.full(stage),
+              ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, mB, sy.full(stage),
                                col0 + c * EC::kMnChunk, k0, b);
           } else {
-            ptx::tma_load_3d(sb, tmB, sy.full(stage), k0, col0, b);
+            ptx::tma_load_3d(sb, mB, sy.full(stage), k0, col0, b);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -487,10 +503,6 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       // (2-SM MMAs: M = 256, the pair's two row tiles at once.)
       constexpr int kMmaM = SM2 ? 2 * kTileM : kTileM;
-      constexpr uint32_t idesc_full = F32 ? ptx::idesc_tf32_f32(kMmaM, kTileN, A_MN, B_MN)
-                                          : ptx::idesc_bf16_f32(kMmaM, kTileN, A_MN, B_MN);
-      constexpr uint32_t idesc_half = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN / 2, A_MN, B_MN)
-                                          : ptx::idesc_bf16_f32(kTileM, kTileN / 2, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -503,13 +515,16 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // diagonal 256-column block with its right half entirely above the
         // diagonal: only its left 128 columns are computed (N = 128).  A 2-SM
         // MMA shares N between the pair's row tiles and always takes 256.
-        uint32_t idesc = idesc_full;
-        if (SYM && !SM2) {
-          int b, I, J;
-          tile_decode(G.space, t - G.tile_begin, &b, &I, &J);
-          I = row_tile(I);
-          if ((I & 1) == 0 && J == (I >> 1)) idesc = idesc_half;
+        bool half_n = false;
+        int tI = 0, tJ = 0;
+        if ((SYM && !SM2) || G.half_a || G.half_b) {
+          int b;
+          tile_decode(G.space, t - G.tile_begin, &b, &tI, &tJ);
+          tI = row_tile(tI);
+          half_n = SYM && !SM2 && (tI & 1) == 0 && tJ == (tI >> 1);
         }
+        const int bnd_a = G.half_a ? 256 * ((tI >> 1) + 1) : 0x7FFFFFFF;
+        const int bnd_b = G.half_b ? 256 * (tJ + 1) : 0x7FFFFFFF;
         if (!detail::wait_bounded<SM2>(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
           break;
         ptx::tc_fence_after();
@@ -523,16 +538,22 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           ptx::tc_fence_after();
           const uint32_t sa = smem_base + stage * R::kStageBytes;
           const uint32_t sb = sa + kABytes;
+          const int k0 = kb * EC::kBlockK;
+          const bool amn = A_MN || k0 >= bnd_a;
+          const bool bmn = B_MN || k0 >= bnd_b;
+          const uint32_t idesc =
+              F32 ? ptx::idesc_tf32_f32(half_n ? kTileM : kMmaM, half_n ? kTileN / 2 : kTileN, amn, bmn)
+                  : ptx::idesc_bf16_f32(half_n ? kTileM : kMmaM, half_n ? kTileN / 2 : kTileN, amn, bmn);
 #pragma unroll
           for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
             // K-major: an MMA's K slice is 32 bytes further along the swizzle
             // row; MN-major: kMmaK k-rows of 128 bytes further down.
             const uint64_t ad =
-                A_MN ? ptx::sw128_desc(sa + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
-                     : ptx::sw128_desc(sa + kk * 32, 16, 1024);
+                amn ? ptx::sw128_desc(sa + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                    : ptx::sw128_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd =
-                B_MN ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
-                     : ptx::sw128_desc(sb + kk * 32, 16, 1024);
+                bmn ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                    : ptx::sw128_desc(sb + kk * 32, 16, 1024);
             if (F32 && SM2)
               ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             else if (F32)
@@ -761,6 +782,15 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           __syncwarp();
           if (lane == 0) {
             ptx::tma_store_3d(tmOut, d, gj0, R0, b);
+            ptx::bulk_commit();
+          }
+        } else if (gj0 < R0 && P.half_out && (gj0 >> 8) != (R0 >> 8)) {
+          // Half storage, outside the diagonal 256-block: the chunk alone.
+          st_row(stg);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(tmOut, stg, gj0, R0, b);
             ptx::bulk_commit();
           }
         } else if (gj0 < R0) {

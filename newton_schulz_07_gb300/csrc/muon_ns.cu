@@ -216,7 +216,14 @@ struct StepIO {
   const float* norms;  // non-null in the first step: X is unscaled
   uint16_t* Xn;        // update output
   uint16_t* Xt;        // update only, optional: the transposed output
+  bool half;           // A and B are half-stored (lower triangle and diagonal 256-blocks)
 };
+
+// The fused bf16 calls store A and B half (each product reads the missing
+// triangle transposed); the per-step entry points keep them full.
+#ifndef MNS_HALF_SYM
+#define MNS_HALF_SYM 1
+#endif
 
 // Launch parameters (about 4 KB) are built on the host and copied at launch.
 mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err) {
@@ -255,6 +262,7 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   const bool T = io[0].p.T, f32 = io[0].p.f32;
   const int bk = block_k(f32), mc = mn_chunk(f32);
   P->round_tf32 = 1;  // A feeds the next product
+  P->half_out = io[0].half ? 1 : 0;
   int max_k = 0;
   for (int i = 0; i < ng; ++i)
     if (io[i].p.n > max_k) max_k = static_cast<int>(io[i].p.n);
@@ -288,6 +296,7 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
   const bool f32 = io[0].p.f32;
   const int bk = block_k(f32);
   P->round_tf32 = 1;  // B feeds the update product
+  P->half_out = io[0].half ? 1 : 0;
   int max_k = 0;
   for (int i = 0; i < ng; ++i)
     if (io[i].p.m > max_k) max_k = static_cast<int>(io[i].p.m);
@@ -297,6 +306,12 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
     set_group(P, i, 1, batch, m, m, m, &total, f32, mode);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
+    if (io[i].half) {
+      // A is half-stored: both operands read its upper part transposed.
+      P->grp[i].half_a = P->grp[i].half_b = 1;
+      if (!make_map(&P->tmA2[i], io[i].A, m, m, batch, mn_chunk(f32), bk, f32)) return MUON_NS_ERR_CUDA;
+      P->tmB2[i] = P->tmA2[i];
+    }
     if (!make_map(&P->tmA[i], io[i].A, m, m, batch, bk, mns::kTileM, f32) ||
         !make_map(&P->tmB[i], io[i].A, m, m, batch, bk, b_box_rows(mode), f32) ||
         !make_out_map(&P->tmOut[i], io[i].B, m, m, batch, f32))
@@ -341,6 +356,13 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     P->grp[i].addend = io[i].X;
     P->grp[i].diag_in = io[i].D;
     P->grp[i].norms = io[i].norms;
+    if (io[i].half) {
+      // B is half-stored: its rows are the A operand (wide) or the B operand
+      // (tall); past the diagonal block they are read transposed.
+      CUtensorMap* alt = T ? &P->tmB2[i] : &P->tmA2[i];
+      (T ? P->grp[i].half_b : P->grp[i].half_a) = 1;
+      if (!make_map(alt, io[i].B, p.m, p.m, p.batch, mc, bk, f32)) return MUON_NS_ERR_CUDA;
+    }
     // Transposed output: [batch][N][M] of this launch's [batch][M][N] output.
     if (io[i].Xt != nullptr &&
         !make_out_map(&P->tmOutT[i], io[i].Xt, T ? p.m : p.n, T ? p.n : p.m, p.batch, f32))
@@ -430,6 +452,7 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
           e.D = reinterpret_cast<float*>(t.ws + t.L.diag);
           e.norms = (k == 0) ? reinterpret_cast<const float*>(t.ws + t.L.norms) : nullptr;
           e.Xn = nxt;
+          e.half = MNS_HALF_SYM && !t.p.f32;
           members[ng++] = i;
         }
         if (ng == 0) continue;
