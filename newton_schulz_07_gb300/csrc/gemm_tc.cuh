@@ -60,6 +60,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -392,43 +393,83 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         I = row_tile(I);
         const int row0 = I * kTileM;
         const int col0 = J * kTileN;
+        // k-block from which an operand of a half-stored matrix is read
+        // transposed (num_kb: never), as in the MMA issuer.
+        const int kb_a = G.half_a ? min(256 * ((I >> 1) + 1) / EC::kBlockK, num_kb) : num_kb;
+        const int kb_b = G.half_b ? min(256 * (J + 1) / EC::kBlockK, num_kb) : num_kb;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded<SM2>(sy.empty(stage), phase ^ 1u, abort_flag, P.err,
-                                         P.budget)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sa = smem_base + stage * R::kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          const int k0 = kb * EC::kBlockK;
-          constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
-          // Operands of a half-stored matrix: past the rows' diagonal 256-block
-          // the k-block is read transposed (MN-major) from the lower triangle.
-          const bool amn = A_MN || (G.half_a && k0 >= 256 * ((I >> 1) + 1));
-          const bool bmn = B_MN || (G.half_b && k0 >= 256 * (J + 1));
-          const CUtensorMap* mA = (amn && !A_MN) ? &P.tmA2[gr] : tmA;
-          const CUtensorMap* mB = (bmn && !B_MN) ? &P.tmB2[gr] : tmB;
-          if (SM2) {
-            // This CTA's A tile and its half of the B panel, into its own
-            // shared memory; all bytes of the pair are counted on CTA 0's
-            // barrier, which expects both CTAs' stages.
-            const uint32_t fb = ptx::mapa(sy.full(stage), 0);
-            if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), 2 * R::kStageBytes);
-            if (amn) {
-#pragma unroll
-              for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
-                ptx::tma_load_3d_pair(sa + c * EC::kMnChunkBytes, mA, fb, row0 + c * EC::kMnChunk, k0, b);
-            } else {
-              ptx::tma_load_3d_pair(sa, mA, fb, k0, row0, b);
+        // Up to three segments of fixed operand majorness, each naming its
+        // tensor maps at compile time (a map chosen per k-block at run time
+        // made every product about 25 % slower on GB300).
+        auto ploop = [&](auto amn_t, auto bmn_t, int kb0, int kb1) {
+          constexpr bool AMN = decltype(amn_t)::value;
+          constexpr bool BMN = decltype(bmn_t)::value;
+          // Past the switch the operand is read through the MN-major map of
+          // the half-stored matrix.
+          const CUtensorMap* mA = (AMN && !A_MN) ? &P.tmA2[gr] : tmA;
+          const CUtensorMap* mB = (BMN && !B_MN) ? &P.tmB2[gr] : tmB;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!detail::wait_bounded<SM2>(sy.empty(stage), phase ^ 1u, abort_flag, P.err,
+                                           P.budget)) {
+              ok = false;
+              return;
             }
-            if (bmn) {
+            const uint32_t sa = smem_base + stage * R::kStageBytes;
+            const uint32_t sb = sa + kABytes;
+            const int k0 = kb * EC::kBlockK;
+            constexpr int kNch = kTileN / EC::kMnChunk;  // MN-major chunks of the B panel
+            if (SM2) {
+              // This CTA's A tile and its half of the B panel, into its own
+              // shared memory; all bytes of the pair are counted on CTA 0's
+              // barrier, which expects both CTAs' stages.
+              const uint32_t fb = ptx::mapa(sy.full(stage), 0);
+              if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), 2 * R::kStageBytes);
+              if (AMN) {
 #pragma unroll
-              for (int c = 0; c < kNch / 2; ++c)
-                ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, mB, fb,
-                                      col0 + (static_cast<int>(crank) * (kNch / 2) + c) * EC::kMnChunk, k0, b);
+                for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
+                  ptx::tma_load_3d_pair(sa + c * EC::kMnChunkBytes, mA, fb, row0 + c * EC::kMnChunk, k0, b);
+              } else {
+                ptx::tma_load_3d_pair(sa, mA, fb, k0, row0, b);
+              }
+              if (BMN) {
+#pragma unroll
+                for (int c = 0; c < kNch / 2; ++c)
+                  ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, mB, fb,
+                                        col0 + (static_cast<int>(crank) * (kNch / 2) + c) * EC::kMnChunk, k0, b);
+              } else {
+                ptx::tma_load_3d_pair(sb, mB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
+              }
             } else {
-              ptx::tma_load_3d_pair(sb, mB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
+              ptx::mbar_arrive_expect_tx(sy.full(stage), R::kStageBytes);
+              if (AMN) {
+#pragma unroll
+                for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
+                  ptx::tma_load_3d(sa + c * EC::kMnChunkBytes, mA, sy.full(stage),
+                                   row0 + c * EC::kMnChunk, k0, b);
+              } else {
+                ptx::tma_load_3d(sa, mA, sy.full(stage), k0, row0, b);
+              }
+              if (CL == 2) {
+                // This CTA's half of the shared panel, into both CTAs.
+                if (BMN) {
+#pragma unroll
+                  for (int c = 0; c < kNch / 2; ++c) {
+                    const int cg = static_cast<int>(crank) * (kNch / 2) + c;
+                    ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, mB, sy.full(stage),
+                                        col0 + cg * EC::kMnChunk, k0, b, 0x3);
+                  }
+                } else {
+                  ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), mB, sy.full(stage), k0,
+                                      col0 + static_cast<int>(crank) * (kTileN / 2), b, 0x3);
+                }
+              } else if (BMN) {
+#pragma unroll
+                for (int c = 0; c < kNch; ++c)
+                  ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, mB, sy.full(stage),
+                                   col0 + c * EC::kMnChunk, k0, b);
+              } else {
+                ptx::tma_load_3d(sb, mB, sy.full(stage), k0, col0, b);
+              }
             }
             issued_mask |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -436,45 +477,21 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               stage = 0;
               phase ^= 1u;
             }
-            continue;
           }
-          ptx::mbar_arrive_expect_tx(sy.full(stage), R::kStageBytes);
-          if (amn) {
-#pragma unroll
-            for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
-              ptx::tma_load_3d(sa + c * EC::kMnChunkBytes, mA, sy.full(stage),
-                               row0 + c * EC::kMnChunk, k0, b);
-          } else {
-            ptx::tma_load_3d(sa, mA, sy.full(stage), k0, row0, b);
-          }
-          if (CL == 2) {
-            // This CTA's half of the shared panel, into both CTAs.
-            if (bmn) {
-#pragma unroll
-              for (int c = 0; c < kNch / 2; ++c) {
-                const int cg = static_cast<int>(crank) * (kNch / 2) + c;
-                ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, mB, sy.full(stage),
-                                    col0 + cg * EC::kMnChunk, k0, b, 0x3);
-              }
-            } else {
-              ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), mB, sy.full(stage), k0,
-                                  col0 + static_cast<int>(crank) * (kTileN / 2), b, 0x3);
-            }
-          } else if (bmn) {
-#pragma unroll
-            for (int c = 0; c < kNch; ++c)
-              ptx::tma_load_3d(sb + c * EC::kMnChunkBytes, mB, sy.full(stage),
-                               col0 + c * EC::kMnChunk, k0, b);
-          } else {
-            ptx::tma_load_3d(sb, mB, sy.full(stage), k0, col0, b);
-          }
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == R::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        };
+        using kA = std::integral_constant<bool, A_MN>;
+        using kB = std::integral_constant<bool, B_MN>;
+        using kT = std::integral_constant<bool, true>;
+        const int s1 = kb_a < kb_b ? kb_a : kb_b;
+        const int s2 = kb_a < kb_b ? kb_b : kb_a;
+        ploop(kA{}, kB{}, 0, s1);
+        if (ok && s2 > s1) {
+          if (kb_a < kb_b)
+            ploop(kT{}, kB{}, s1, s2);
+          else
+            ploop(kA{}, kT{}, s1, s2);
         }
+        if (ok && num_kb > s2) ploop(kT{}, kT{}, s2, num_kb);
         if (!ok) break;
       }
       // Wait for every copy still in flight before the CTA can exit (with
@@ -523,57 +540,78 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           tI = row_tile(tI);
           half_n = SYM && !SM2 && (tI & 1) == 0 && tJ == (tI >> 1);
         }
-        const int bnd_a = G.half_a ? 256 * ((tI >> 1) + 1) : 0x7FFFFFFF;
-        const int bnd_b = G.half_b ? 256 * (tJ + 1) : 0x7FFFFFFF;
+        // k-block from which an operand of a half-stored matrix is read
+        // transposed (num_kb: never).
+        const int kb_a = G.half_a ? min(256 * ((tI >> 1) + 1) / EC::kBlockK, num_kb) : num_kb;
+        const int kb_b = G.half_b ? min(256 * (tJ + 1) / EC::kBlockK, num_kb) : num_kb;
         if (!detail::wait_bounded<SM2>(sy.tempty(buf), tphase ^ 1u, abort_flag, P.err, P.budget))
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!detail::wait_bounded<SM2>(sy.full(stage), phase, abort_flag, P.err, P.budget)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t sa = smem_base + stage * R::kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          const int k0 = kb * EC::kBlockK;
-          const bool amn = A_MN || k0 >= bnd_a;
-          const bool bmn = B_MN || k0 >= bnd_b;
-          const uint32_t idesc =
-              F32 ? ptx::idesc_tf32_f32(half_n ? kTileM : kMmaM, half_n ? kTileN / 2 : kTileN, amn, bmn)
-                  : ptx::idesc_bf16_f32(half_n ? kTileM : kMmaM, half_n ? kTileN / 2 : kTileN, amn, bmn);
+        // The main loop runs in up to three segments of fixed operand
+        // majorness, so that the descriptors stay compile-time constants: the
+        // tensor pipe is fed from this one thread.
+        auto kloop = [&](auto amn_t, auto bmn_t, int kb0, int kb1) {
+          constexpr bool AMN = decltype(amn_t)::value;
+          constexpr bool BMN = decltype(bmn_t)::value;
+          constexpr uint32_t id_full = F32 ? ptx::idesc_tf32_f32(kMmaM, kTileN, AMN, BMN)
+                                           : ptx::idesc_bf16_f32(kMmaM, kTileN, AMN, BMN);
+          constexpr uint32_t id_half = F32 ? ptx::idesc_tf32_f32(kTileM, kTileN / 2, AMN, BMN)
+                                           : ptx::idesc_bf16_f32(kTileM, kTileN / 2, AMN, BMN);
+          const uint32_t idesc = half_n ? id_half : id_full;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!detail::wait_bounded<SM2>(sy.full(stage), phase, abort_flag, P.err, P.budget)) {
+              ok = false;
+              return;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = smem_base + stage * R::kStageBytes;
+            const uint32_t sb = sa + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
-            // K-major: an MMA's K slice is 32 bytes further along the swizzle
-            // row; MN-major: kMmaK k-rows of 128 bytes further down.
-            const uint64_t ad =
-                amn ? ptx::sw128_desc(sa + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
-                    : ptx::sw128_desc(sa + kk * 32, 16, 1024);
-            const uint64_t bd =
-                bmn ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
-                    : ptx::sw128_desc(sb + kk * 32, 16, 1024);
-            if (F32 && SM2)
-              ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else if (F32)
-              ptx::mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else if (SM2)
-              ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
+              // K-major: an MMA's K slice is 32 bytes further along the swizzle
+              // row; MN-major: kMmaK k-rows of 128 bytes further down.
+              const uint64_t ad =
+                  AMN ? ptx::sw128_desc(sa + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                      : ptx::sw128_desc(sa + kk * 32, 16, 1024);
+              const uint64_t bd =
+                  BMN ? ptx::sw128_desc(sb + kk * EC::kMnStep, EC::kMnChunkBytes, 1024)
+                      : ptx::sw128_desc(sb + kk * 32, 16, 1024);
+              if (F32 && SM2)
+                ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              else if (F32)
+                ptx::mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              else if (SM2)
+                ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              else
+                ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            if (SM2)
+              ptx::mma_commit_pair(sy.empty(stage), 0x3);
+            else if (CL == 2)
+              ptx::mma_commit_mc(sy.empty(stage), 0x3);
             else
-              ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_commit(sy.empty(stage));
+            if (++stage == R::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          if (SM2)
-            ptx::mma_commit_pair(sy.empty(stage), 0x3);
-          else if (CL == 2)
-            ptx::mma_commit_mc(sy.empty(stage), 0x3);
+        };
+        using kA = std::integral_constant<bool, A_MN>;
+        using kB = std::integral_constant<bool, B_MN>;
+        using kT = std::integral_constant<bool, true>;
+        const int s1 = kb_a < kb_b ? kb_a : kb_b;
+        const int s2 = kb_a < kb_b ? kb_b : kb_a;
+        kloop(kA{}, kB{}, 0, s1);
+        if (ok && s2 > s1) {
+          if (kb_a < kb_b)
+            kloop(kT{}, kB{}, s1, s2);
           else
-            ptx::mma_commit(sy.empty(stage));
-          if (++stage == R::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+            kloop(kA{}, kT{}, s1, s2);
         }
+        if (ok && num_kb > s2) kloop(kT{}, kT{}, s2, num_kb);
         if (!ok) break;
         if (SM2)
           ptx::mma_commit_pair(sy.tfull(buf), 0x3);

@@ -44,6 +44,8 @@ def test_graph_capture_and_replay_matches_eager(shape):
     assert ns.read_error(ws) == 0
 
 
+# The refused call launches nothing, so the capture ends empty.
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_cached_workspace_does_not_grow_during_capture():
     big = (2, 2048, 3072)  # larger than anything the cache has held in this test process
     G = torch.zeros(big, dtype=torch.bfloat16, device="cuda")
