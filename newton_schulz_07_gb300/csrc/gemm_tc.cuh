@@ -152,6 +152,13 @@ __device__ __forceinline__ uint32_t stage_off32(int row, int col) {
   return static_cast<uint32_t>(row * 128 + g * 16 + (col & 3) * 4);
 }
 
+// Byte offset of 16-byte granule `g` (0..7) of row `row` of a 32 x 64 bf16
+// staging box: rows of 128 bytes, granule XOR (row & 7) (the 128-byte TMA
+// swizzle, on a 1024-byte aligned buffer).
+__device__ __forceinline__ uint32_t stage_off_wide(int row, int g) {
+  return static_cast<uint32_t>(row * 128 + ((g ^ (row & 7)) << 4));
+}
+
 // Round an fp32 value to the nearest tf32 (10-bit mantissa, ties to even),
 // kept in fp32 storage: the tensor core reads tf32 by dropping the low 13
 // bits, so values stored this way reach it exactly.  Inputs here are finite.
@@ -639,6 +646,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     constexpr int kBufs = R::kBufs;
     constexpr int kCB = EC::kChunkBytes;
     constexpr int kAV = EC::kAddVec;  // 16-byte addend vectors per lane and chunk
+    // The 4-warp bf16 update stores 32 x 64 boxes (update_epi_warps).
+    constexpr bool kWide = !SYM && !F32 && EPI_WARPS == 4;
+    static_assert(!kWide || (kBufs * kCB == 4096 && kChunksPerWarp % 2 == 0), "wide staging box");
     const uint32_t stg = smem_base + R::kStages * R::kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
     int buf = 0;
     uint32_t tphase = 0;
@@ -794,11 +804,35 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // stores (rows beyond M or columns beyond N are clipped by the TMA).
         const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
         if (lane == 0) {
-          if (kBufs == 2 && !SYM && !P.out_t) ptx::bulk_wait_read<1>();
-          else ptx::bulk_wait_read<0>();
+          if (kWide) {
+            if (!(cc & 1)) ptx::bulk_wait_read<0>();
+          } else if (kBufs == 2 && !SYM && !P.out_t) {
+            ptx::bulk_wait_read<1>();
+          } else {
+            ptx::bulk_wait_read<0>();
+          }
         }
         __syncwarp();
-        if (!SYM && P.out_t) {
+        if (kWide) {
+          // Chunks 2k and 2k + 1 fill one 32 x 64 box (4 KB, 128-byte rows):
+          // the even chunk waited above for the previous box's read; the odd
+          // chunk, or a last even one, stores the box.  Columns past N (the
+          // unwritten half of a last even chunk's box) are clipped by the TMA.
+          const int h = cc & 1;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(stg + stage_off_wide(lane, h * 4 + g), w[4 * g], w[4 * g + 1],
+                              w[4 * g + 2], w[4 * g + 3]);
+          const bool more = cc + 1 < n_chunks && gj0 + 32 < G.N;
+          if (h == 1 || !more) {
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(tmOut, stg, gj0 - h * 32, R0, b);
+              ptx::bulk_commit();
+            }
+          }
+        } else if (!SYM && P.out_t) {
           // The chunk at (R0, gj0) and its transpose at (gj0, R0) of the
           // transposed output.
           const uint32_t d = stg;

@@ -36,6 +36,15 @@ inline PairMode pair_mode(bool f32, int max_k) {
   return f32 ? kSingle : kMulticast;
 }
 
+// Epilogue warps of a bf16 update launch: 8 for short contractions on
+// multicast pairs, 4 otherwise.  The 4-warp bf16 update writes its output in
+// 32 x 64 boxes (128-byte rows, 128-byte swizzle); every other product writes
+// 32 x 32 chunks.  The launcher instantiates, and the host builds the output
+// tensor map, from this one function.
+inline int update_epi_warps(PairMode mode, int max_k) {
+  return (mode != kPairMma && max_k <= kShortK) ? 8 : 4;
+}
+
 // `max_k` is the largest contraction of the launch's groups: short
 // contractions use 8 epilogue warps in the update.
 // Gram / polynomial products: lower-triangle tiles, mirrored stores.

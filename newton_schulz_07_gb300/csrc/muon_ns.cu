@@ -186,12 +186,14 @@ bool make_map(CUtensorMap* map, const void* base, long long inner, long long row
 
 // ---------------------------------------------------------------- launches --
 
-// Output map: [batch][M][N], 32 x 32 boxes; 64-byte swizzle for bf16 (rows of
-// 64 bytes), 128-byte for fp32.
+// Output map: [batch][M][N], 32-row boxes of 128-byte rows with the 128-byte
+// swizzle (fp32 32 x 32, or bf16 32 x 64 for `wide` outputs), or of 64-byte
+// rows with the 64-byte swizzle (bf16 32 x 32).
 bool make_out_map(CUtensorMap* map, const void* base, long long M, long long N, long long batch,
-                  bool f32) {
-  return make_map(map, base, N, M, batch, 32, 32, f32,
-                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                  bool f32, bool wide = false) {
+  const bool b128 = f32 || wide;
+  return make_map(map, base, N, M, batch, (wide && !f32) ? 64 : 32, 32, f32,
+                  b128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // K per pipeline stage and M/N elements per 128-byte row (the TMA box sizes).
@@ -336,6 +338,9 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   for (int i = 0; i < ng; ++i)
     if (io[i].p.m > max_k) max_k = static_cast<int>(io[i].p.m);
   const mns::PairMode mode = mns::pair_mode(f32, max_k);
+  // The 4-warp bf16 update writes 32 x 64 output boxes.
+  const bool wide_out = !f32 && mns::update_epi_warps(mode, max_k) == 4;
+  if (!f32 && P->out_t) return MUON_NS_ERR_INVALID_ARG;  // transposed outputs are fp32 only
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
     if (!T) {
@@ -343,14 +348,14 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
       set_group(P, i, 0, p.batch, p.m, p.n, p.m, &total, f32, mode);
       if (!make_map(&P->tmA[i], io[i].B, p.m, p.m, p.batch, bk, mns::kTileM, f32) ||
           !make_map(&P->tmB[i], io[i].X, p.n, p.m, p.batch, mc, bk, f32) ||
-          !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch, f32))
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.m, p.n, p.batch, f32, wide_out))
         return MUON_NS_ERR_CUDA;
     } else {
       // Yn [n][m] = a Y + Y B: A operand = rows of Y, B operand = rows of B (= columns).
       set_group(P, i, 0, p.batch, p.n, p.m, p.m, &total, f32, mode);
       if (!make_map(&P->tmA[i], io[i].X, p.m, p.n, p.batch, bk, mns::kTileM, f32) ||
           !make_map(&P->tmB[i], io[i].B, p.m, p.m, p.batch, bk, b_box_rows(mode), f32) ||
-          !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch, f32))
+          !make_out_map(&P->tmOut[i], io[i].Xn, p.n, p.m, p.batch, f32, wide_out))
         return MUON_NS_ERR_CUDA;
     }
     P->grp[i].addend = io[i].X;
