@@ -136,7 +136,13 @@ int muon_ns_workspace_region(int batch, int rows, int cols, int region, size_t* 
  * first step reads G itself and applies s = 1 / (||G||_F + eps) in its
  * epilogues (A0 = s^2 G G^T, X1 = s (a + D) G + s O G), so no scaled copy of G
  * is made and X0 is never rounded to bf16.  In place with an odd step count
- * the result is copied once from the workspace into out at the end. */
+ * the result is copied once from the workspace into out at the end.
+ * For stacks of two or more matrices each product kernel waits for the
+ * previous product of the same matrix (per-matrix completion counters in the
+ * workspace, bounded waits that report MUON_NS_ERR_TIMEOUT through the error
+ * word) rather than for the whole previous kernel, so consecutive kernels
+ * overlap; the call's last kernel still completes after all the others, so
+ * work queued after the call on `stream` sees every result. */
 int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
                const float* coeffs, float eps, void* workspace, size_t workspace_bytes,
                cudaStream_t stream);

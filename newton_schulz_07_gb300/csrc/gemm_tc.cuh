@@ -198,7 +198,21 @@ struct GroupArgs {
   // of the product that wrote it): k-blocks past the operand rows' diagonal
   // 256-block are read transposed, MN-major, through tmA2 / tmB2.
   int half_a, half_b;
+  // Per-matrix completion counters of a whole NS call (both optional):
+  //   dep_sig   every finished unit adds kDepUnit to dep_sig[b] once its
+  //             outputs are written (each epilogue warp of the unit's CTAs
+  //             adds its share);
+  //   dep_wait  the unit's operands and addend come from the previous product
+  //             of the same matrix: it waits until dep_wait[b] >= dep_target
+  //             (GemmParams::dep_flags), not for the whole previous grid.
+  int* dep_sig;
+  const int* dep_wait;
+  int dep_target;
 };
+
+// Counter increment per finished unit of the tile space, whatever the
+// launch's CTAs per unit and epilogue warps.
+constexpr int kDepUnit = 16;
 
 struct GemmParams {
   CUtensorMap tmA[kMaxGroups];    // A operand (rows of the output)
@@ -221,6 +235,11 @@ struct GemmParams {
   // 256 x 256 block; elsewhere only the lower triangle is written, and
   // consumers read the upper part from it transposed (GroupArgs::half_a/b).
   int half_out;
+  // Waits are per matrix (GroupArgs::dep_wait): the kernel starts on matrices
+  // whose inputs are ready while the previous grid still runs, and waits for
+  // the previous grid only before it exits, so that its completion still
+  // implies that of every earlier kernel in the stream.
+  int dep_flags;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -275,6 +294,44 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait until a per-matrix completion counter reaches `target`
+// (acquire at GPU scope).  Gives up early once any kernel has set the error
+// word: the counter may then never get there.
+__device__ __forceinline__ bool wait_count(const int* c, int target, volatile int* abort_flag,
+                                           int* err, long long budget) {
+  if (ptx::ld_acquire_gpu(c) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(64);
+    if (ptx::ld_acquire_gpu(c) >= target) return true;
+    if (*abort_flag) return false;
+    if (err != nullptr && *reinterpret_cast<volatile int*>(err) != 0) {
+      *abort_flag = 1;
+      return false;
+    }
+    if (clock64() - t0 > budget) {
+      raise_error(abort_flag, err);
+      return false;
+    }
+  }
+}
+
+// Bounded wait until the producer has seen the inputs of `units` units
+// complete (CTA-scope acquire of its shared-memory count).
+__device__ __forceinline__ bool wait_seen(uint32_t addr, int units, volatile int* abort_flag,
+                                          int* err, long long budget) {
+  if (ptx::ld_acquire_cta_shared(addr) >= units) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::ld_acquire_cta_shared(addr) >= units) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > budget) {
+      raise_error(abort_flag, err);
+      return false;
+    }
+  }
+}
+
 // Bounded wait used on the way out: ignores the abort flag.
 template <bool CLUSTER = false>
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long budget) {
@@ -307,6 +364,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  // Units whose inputs the producer has seen complete (per-matrix counters),
+  // handed to the epilogue warps by a CTA-scope release.
+  __shared__ int dep_seen_sh;
   constexpr int kEpiWarps = Epi<EPI_WARPS>::kWarps;
   constexpr int kEpiThreads = Epi<EPI_WARPS>::kThreads;
   constexpr int kChunksPerWarp = Epi<EPI_WARPS>::kChunksPerWarp;
@@ -346,6 +406,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ptx::mbar_init(sy.tempty(1), SM2 ? 2 * kEpiWarps : kEpiThreads);
     ptx::mbar_init(sy.mma_done(), 1);
     *abort_flag = 0;
+    dep_seen_sh = 0;
     ptx::fence_barrier_init();
     for (int g = 0; g < P.num_groups; ++g) {
       ptx::prefetch_tensormap(&P.tmA[g]);
@@ -378,7 +439,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
   // meanwhile.  Nothing produced by the previous kernel is touched before this
   // grid's dependency has completed.
   ptx::griddep_launch_dependents();
-  ptx::griddep_wait();
+  if (!P.dep_flags) ptx::griddep_wait();
 
   const long long total = P.total_tiles;
 
@@ -389,6 +450,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0;   // stages with a load issued at least once
       uint32_t issued_phase = 0;  // parity of the last load issued per stage
+      int units_seen = 0;         // units whose inputs are known complete
       for (long long t = unit0; t < total; t += ustride) {
         const int gr = find_group(P, t);
         const GroupArgs& G = P.grp[gr];
@@ -404,6 +466,14 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // transposed (num_kb: never), as in the MMA issuer.
         const int kb_a = G.half_a ? min(256 * ((I >> 1) + 1) / EC::kBlockK, num_kb) : num_kb;
         const int kb_b = G.half_b ? min(256 * (J + 1) / EC::kBlockK, num_kb) : num_kb;
+        // The operands of matrix b are complete once the previous product
+        // has finished all of its units.  Every unit is then counted for the
+        // epilogue, which reads the same inputs' addend and diagonal.
+        if (G.dep_wait != nullptr) {
+          if (!detail::wait_count(G.dep_wait + b, G.dep_target, abort_flag, P.err, P.budget)) break;
+          ptx::fence_proxy_async_global();
+        }
+        ptx::st_release_cta_shared(ptx::smem_u32(&dep_seen_sh), ++units_seen);
         bool ok = true;
         // Up to three segments of fixed operand majorness, each naming its
         // tensor maps at compile time (a map chosen per k-block at run time
@@ -652,6 +722,13 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     const uint32_t stg = smem_base + R::kStages * R::kStageBytes + static_cast<uint32_t>(e * kBufs * kCB);
     int buf = 0;
     uint32_t tphase = 0;
+    // Completion counter of the last unit, published by lane 0 once its bulk
+    // stores have completed; every epilogue warp of the unit's CTAs adds
+    // kSigShare, kDepUnit in all.
+    constexpr int kSigShare = kDepUnit / (CL * kEpiWarps);
+    static_assert(kSigShare * CL * kEpiWarps == kDepUnit, "counter share");
+    int* pend_sig = nullptr;
+    int units_done = 0;  // units of this CTA taken so far (as counted by the producer)
     for (long long t = unit0; t < total; t += ustride) {
       const int gr = find_group(P, t);
       const GroupArgs& G = P.grp[gr];
@@ -666,6 +743,23 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       int ready = 0;
       if (lane == 0)
         ready = detail::wait_bounded<SM2>(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
+      // The previous unit's stores have long completed (this unit's main
+      // loop ran meanwhile): publish it.  The addend, diagonal and norms read
+      // below come from earlier products of matrix b, and the buffers written
+      // below were read by them: the producer's acquire of their counter is
+      // passed on through shared memory.
+      if (lane == 0 && ready) {
+        if (pend_sig != nullptr) {
+          ptx::bulk_wait_all();
+          ptx::fence_proxy_async_global();
+          ptx::red_release_gpu_add(pend_sig, kSigShare);
+          pend_sig = nullptr;
+        }
+        if (G.dep_wait != nullptr &&
+            !detail::wait_seen(ptx::smem_u32(&dep_seen_sh), units_done + 1, abort_flag, P.err, P.budget))
+          ready = 0;
+      }
+      ++units_done;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       __syncwarp();
@@ -682,11 +776,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
       // Addend coefficient: per row (row-indexed diagonal or none) ...
       float mscale = 1.0f;  // per-matrix scale of unscaled operands
-      if (G.norms != nullptr) mscale = 1.0f / (__ldg(G.norms + b) + P.eps);
+      if (G.norms != nullptr) mscale = 1.0f / (ptx::ld_global_f32(G.norms + b) + P.eps);
       const float alpha_t = SYM ? P.alpha * (mscale * mscale) : P.alpha * mscale;
       float row_coef = P.beta;
       if (!SYM && G.diag_in != nullptr && !P.diag_per_col && row_ok)
-        row_coef += __ldg(G.diag_in + static_cast<long long>(b) * G.M + gi);
+        row_coef += ptx::ld_global_f32(G.diag_in + static_cast<long long>(b) * G.M + gi);
       row_coef *= mscale;
       // ... or per column, staged in shared memory for this warp's columns.
       const bool col_mode = !SYM && G.diag_in != nullptr && P.diag_per_col;
@@ -695,14 +789,17 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         for (int v = 0; v < kChunksPerWarp; ++v) {
           const int col = col_base + v * 32 + lane;
           colc[v * 32 + lane] =
-              (P.beta + (col < G.N ? __ldg(G.diag_in + static_cast<long long>(b) * G.N + col) : 0.0f)) *
+              (P.beta + (col < G.N ? ptx::ld_global_f32(G.diag_in + static_cast<long long>(b) * G.N + col) : 0.0f)) *
               mscale;
         }
         __syncwarp();
       }
       // Addend values of one chunk (kAV 16-byte vectors of 8 bf16 or 4 fp32),
       // prefetched one chunk ahead so their latency overlaps the previous
-      // chunk's work.
+      // chunk's work.  The addend, diagonal and norms are read with plain
+      // (coherent) global loads: in a whole call the kernel that wrote them
+      // may still be running, which the non-coherent read-only path does not
+      // allow.
       constexpr int kPer = 16 / EC::kBytes;  // elements per 16-byte vector
       auto load_addend = [&](int cc, uint4 (&dst)[kAV]) {
         const int gj0 = col_base + cc * 32;
@@ -712,7 +809,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const uint4* src = reinterpret_cast<const uint4*>(addm + (gi * G.ld + gj0) * EC::kBytes);
 #pragma unroll
         for (int g = 0; g < kAV; ++g)
-          if (gj0 + kPer * g + kPer <= G.N) dst[g] = __ldg(src + g);
+          if (gj0 + kPer * g + kPer <= G.N) dst[g] = ptx::ld_global_v4(src + g);
       };
       // Staging-chunk offset of element (row, col) for this element type.
       auto soff = [](int row, int col) -> uint32_t {
@@ -912,11 +1009,18 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       } else {
         ptx::mbar_arrive(sy.tempty(buf));
       }
+      if (lane == 0 && G.dep_sig != nullptr) pend_sig = G.dep_sig + b;
       buf ^= 1;
       if (buf == 0) tphase ^= 1u;
     }
     // Staging buffers stay valid until every bulk store of this warp is done.
-    if (lane == 0) ptx::bulk_wait_all();
+    if (lane == 0) {
+      ptx::bulk_wait_all();
+      if (pend_sig != nullptr && !*abort_flag) {
+        ptx::fence_proxy_async_global();
+        ptx::red_release_gpu_add(pend_sig, kSigShare);
+      }
+    }
     __syncwarp();
   }
 
@@ -932,6 +1036,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     else
       ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (P.dep_flags) ptx::griddep_wait();
 }
 
 }  // namespace mns

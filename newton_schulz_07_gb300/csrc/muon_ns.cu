@@ -18,6 +18,7 @@
 // The iterate ping-pongs between the workspace and `out`, starting where the
 // parity of `steps` makes the last step write `out`; only in place
 // (out == G) with an odd step count is the result copied once at the end.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -47,7 +48,9 @@ struct Problem {
 };
 
 struct Layout {
-  size_t error, tickets, partials, norms, diag, x, a, b, total;
+  // deps: per-matrix completion counters of the three products (int [3][batch]),
+  // right after the norm kernel's tickets so that one memset clears both.
+  size_t error, tickets, deps, partials, norms, diag, x, a, b, total;
   size_t y2, w;  // fp32 mode only: a second tall-orientation iterate and the wide copy
   size_t x_bytes, a_bytes;
   int chunks;
@@ -81,7 +84,8 @@ Layout make_layout(const Problem& p) {
   L.error = off;
   off += 256;
   L.tickets = off;
-  off = round_up(off + 4 * static_cast<size_t>(p.batch), 256);
+  L.deps = off + 4 * static_cast<size_t>(p.batch);
+  off = round_up(off + 16 * static_cast<size_t>(p.batch), 256);
   L.partials = off;
   off = round_up(off + 4 * static_cast<size_t>(p.batch) * L.chunks, 256);
   L.norms = off;
@@ -219,12 +223,42 @@ struct StepIO {
   uint16_t* Xn;        // update output
   uint16_t* Xt;        // update only, optional: the transposed output
   bool half;           // A and B are half-stored (lower triangle and diagonal 256-blocks)
+  // Optional per-matrix completion counters int [3][batch] (Gram, poly,
+  // update), cleared at the start of the call, and the step index: each
+  // product waits for the previous product of the same matrix through them
+  // instead of for the whole previous kernel.
+  int* dep;
+  int step;
 };
+
+// Counter value per matrix after one step of a product: its units per matrix
+// (CTA pairs for bf16) times the kernel's increment per unit.
+long long dep_per_step(int sym, long long M, long long N) {
+  return mns::make_tile_space(sym, 1, static_cast<int>(M), static_cast<int>(N), 1).total *
+         static_cast<long long>(mns::kDepUnit);
+}
+long long dep_per_step_sym(const Problem& p) { return dep_per_step(1, p.m, p.m); }
+
+// A launch waits through counters only if every group has them; otherwise
+// it waits for the whole previous kernel (its groups still signal).
+bool all_have_dep(const StepIO* io, int ng) {
+  for (int i = 0; i < ng; ++i)
+    if (io[i].dep == nullptr) return false;
+  return true;
+}
+long long dep_per_step_update(const Problem& p) {
+  return p.T ? dep_per_step(0, p.n, p.m) : dep_per_step(0, p.m, p.n);
+}
 
 // The fused bf16 calls store A and B half (each product reads the missing
 // triangle transposed); the per-step entry points keep them full.
 #ifndef MNS_HALF_SYM
 #define MNS_HALF_SYM 1
+#endif
+// Whole calls order their products through per-matrix counters (StepIO::dep);
+// MNS_DEP_FLAGS=0 orders them by whole kernels.
+#ifndef MNS_DEP_FLAGS
+#define MNS_DEP_FLAGS 1
 #endif
 
 // Launch parameters (about 4 KB) are built on the host and copied at launch.
@@ -273,6 +307,13 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
     const Problem& p = io[i].p;
     set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32, mode);
     P->grp[i].norms = io[i].norms;
+    // Signals the Gram counter; waits for the previous step's update.
+    if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep;
+    if (all_have_dep(io, ng) && io[i].step > 0) {
+      P->grp[i].dep_wait = io[i].dep + 2 * p.batch;
+      P->grp[i].dep_target = static_cast<int>(io[i].step * dep_per_step_update(p));
+      P->dep_flags = 1;
+    }
     if (!make_out_map(&P->tmOut[i], io[i].A, p.m, p.m, p.batch, f32)) return MUON_NS_ERR_CUDA;
     if (!T) {
       // X [batch][m][n]: rows of X are the K-major operand rows.
@@ -308,6 +349,13 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
     set_group(P, i, 1, batch, m, m, m, &total, f32, mode);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
+    // Signals the poly counter; waits for this step's Gram.
+    if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + batch;
+    if (all_have_dep(io, ng)) {
+      P->grp[i].dep_wait = io[i].dep;
+      P->grp[i].dep_target = static_cast<int>((io[i].step + 1) * dep_per_step_sym(io[i].p));
+      P->dep_flags = 1;
+    }
     if (io[i].half) {
       // A is half-stored: both operands read its upper part transposed.
       P->grp[i].half_a = P->grp[i].half_b = 1;
@@ -361,6 +409,13 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     P->grp[i].addend = io[i].X;
     P->grp[i].diag_in = io[i].D;
     P->grp[i].norms = io[i].norms;
+    // Signals the update counter; waits for this step's polynomial.
+    if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + 2 * p.batch;
+    if (all_have_dep(io, ng)) {
+      P->grp[i].dep_wait = io[i].dep + p.batch;
+      P->grp[i].dep_target = static_cast<int>((io[i].step + 1) * dep_per_step_sym(p));
+      P->dep_flags = 1;
+    }
     if (io[i].half) {
       // B is half-stored: its rows are the A operand (wide) or the B operand
       // (tall); past the diagonal block they are read transposed.
@@ -382,10 +437,12 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
                      : mns::launch_full_kmn(*P, mode, max_k, grid, st));
 }
 
+// `clear`: zero the tickets first (callers that clear them together with the
+// dependency counters pass false).
 int run_normalize(const Problem& p, const Layout& L, const void* G, void* X, float eps,
-                  uint8_t* ws, cudaStream_t st) {
+                  uint8_t* ws, cudaStream_t st, bool clear = true) {
   const long long vec = p.R * p.C / (p.f32 ? 4 : 8);
-  if (cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
+  if (clear && cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
   if (mns::launch_pdl(p.f32 ? mns::ns_norm_partial<true> : mns::ns_norm_partial<false>, grid, dim3(mns::kNormThreads), 0, st,
@@ -425,10 +482,15 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
   }
   // Norms only; the first step reads G itself and applies s = 1/(norm + eps)
   // in its epilogues (A0 = s^2 G G^T, X1 = s O G + s (a + D) G), so no scaled
-  // copy of G is written or read.
-  for (int i = 0; i < ns; ++i)
-    if ((s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st)) != MUON_NS_OK)
+  // copy of G is written or read.  One memset clears each stack's norm
+  // tickets and its dependency counters.
+  for (int i = 0; i < ns; ++i) {
+    if (cudaMemsetAsync(S[i].ws + S[i].L.tickets, 0, 16 * static_cast<size_t>(S[i].p.batch), st) !=
+        cudaSuccess)
+      return MUON_NS_ERR_CUDA;
+    if ((s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st, false)) != MUON_NS_OK)
       return s;
+  }
   StepIO io[mns::kMaxGroups];
   int members[mns::kMaxGroups];
   for (int k = 0; k < steps; ++k) {
@@ -458,6 +520,14 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
           e.norms = (k == 0) ? reinterpret_cast<const float*>(t.ws + t.L.norms) : nullptr;
           e.Xn = nxt;
           e.half = MNS_HALF_SYM && !t.p.f32;
+          e.step = k;
+          // A single matrix gains nothing (its next product needs all of
+          // it).  Counters stay far below 2^31 for any realistic step count;
+          // past that, products wait for whole kernels.
+          const long long peak = static_cast<long long>(steps) *
+                                 std::max(dep_per_step_sym(t.p), dep_per_step_update(t.p));
+          if (MNS_DEP_FLAGS && !t.p.f32 && t.p.batch > 1 && peak < (1LL << 30))
+            e.dep = reinterpret_cast<int*>(t.ws + t.L.deps);
           members[ng++] = i;
         }
         if (ng == 0) continue;

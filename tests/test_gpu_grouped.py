@@ -38,6 +38,20 @@ def test_grouped_equals_separate_calls_bitwise(steps):
         np.testing.assert_array_equal(to_bits(o), to_bits(alone(G, steps)))
 
 
+def test_grouped_long_contractions_mixed_batches_bitwise():
+    # Contractions above 1024 (2-SM pairs) with a single-matrix stack in the
+    # same launches as multi-matrix stacks: the latter order their products
+    # through per-matrix counters, the former through whole kernels.
+    shapes = [(2, 1040, 1280), (1, 1032, 1032), (3, 1280, 1040)]
+    Gs = [to_dev(random_bits(s, seed=320 + i)) for i, s in enumerate(shapes)]
+    ws = torch.empty(ns.grouped_workspace_size(Gs), dtype=torch.uint8, device="cuda")
+    outs = ns.muon_ns_grouped(Gs, steps=3, workspace=ws)
+    torch.cuda.synchronize()
+    assert ns.read_error(ws) == 0
+    for G, o in zip(Gs, outs):
+        np.testing.assert_array_equal(to_bits(o), to_bits(alone(G, 3)))
+
+
 def test_grouped_more_than_eight_stacks_and_in_place():
     shapes = [(2, 128 + 8 * i, 256) for i in range(10)] + [(1, 512, 256), (1, 264, 136)]
     Gs = [to_dev(random_bits(s, seed=400 + i)) for i, s in enumerate(shapes)]

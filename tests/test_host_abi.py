@@ -216,6 +216,18 @@ def test_paired_grid_schedule_covers_every_tile_once(M, N):
     assert len(ts) == len(set(ts)) and set(ts) == expect
 
 
+@pytest.mark.parametrize("kind,M,N", [(2, 1536, 1536), (2, 1000, 1000), (2, 8, 8), (3, 1536, 2048),
+                                      (3, 2048, 768), (3, 1096, 1304), (3, 136, 264)])
+def test_paired_units_per_matrix_match_single_matrix_count(kind, M, N):
+    # A whole call's per-matrix completion counters expect, after each step of
+    # a product, the single-matrix unit count of its tile space (times a fixed
+    # increment per unit): every matrix of a stack must own exactly that many.
+    batch = 3
+    per = _lib.lib().muon_ns_tile_count(kind, 1, M, N)
+    counts = np.bincount([b for b, _, _ in tiles(kind, batch, M, N)], minlength=batch)
+    assert per > 0 and list(counts) == [per] * batch
+
+
 def test_paired_tile_counts():
     L = _lib.lib()
     assert L.muon_ns_tile_count(2, 128, 1536, 1536) == 128 * 21  # 6 pair rows: 6 * 7 / 2
