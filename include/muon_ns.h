@@ -261,6 +261,24 @@ int muon_ns_read_error(const void* workspace, int* device_error, int clear, cuda
  * device).  *device_error = 0 if no cached workspace exists yet. */
 int muon_ns_cached_error(int device, int* device_error);
 
+/* Budget of every bounded wait inside the kernels (barrier phases, per-matrix
+ * counters), in SM clock cycles (clock64); 0 restores the default of 4e9
+ * cycles, about 2 s at 2 GHz.  A wait that runs out sets the error word
+ * (read as MUON_NS_ERR_TIMEOUT) and its kernel returns; a budget shorter than
+ * the waits of a healthy call gives spurious timeouts, never a hang.  Applies
+ * to calls made afterwards, from any thread.  MUON_NS_ERR_INVALID_ARG if
+ * cycles < 0. */
+int muon_ns_set_wait_budget(long long cycles);
+
+/* Host-side fault injection for tests of the bounded waits.  With `enable`
+ * nonzero, later whole calls of stacks with two or more matrices give the
+ * first step's polynomial kernel a completion target one unit above what the
+ * Gram kernel signals: its waits run out, every later kernel of the call gives
+ * up when it sees the error word, and the call reports MUON_NS_ERR_TIMEOUT
+ * through it.  Nothing faults; the device stays usable.  Off by default;
+ * returns MUON_NS_OK. */
+int muon_ns_inject_stall(int enable);
+
 /* ---------------------------------------------------------------------------
  * The steps of the path, one kernel each (the same kernels muon_ns_ws runs).
  * `device_error` is an optional device int32 that receives

@@ -16,6 +16,7 @@ from .ns import (  # noqa: F401
     muon_ns_gram,
     muon_ns_grouped,
     grouped_workspace_size,
+    inject_stall,
     host_workspace_size,
     muon_ns_host,
     muon_ns_normalize,
@@ -23,6 +24,7 @@ from .ns import (  # noqa: F401
     muon_ns_poly,
     muon_ns_update,
     read_error,
+    set_wait_budget,
     workspace_region,
     workspace_size,
 )

@@ -52,6 +52,8 @@ SIGNATURES = {
     "muon_ns_host": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _c_int, _vp, _c_sz, _vp]),
     "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),
     "muon_ns_cached_error": (_c_int, [_c_int, _pi]),
+    "muon_ns_set_wait_budget": (_c_int, [_c_ll]),
+    "muon_ns_inject_stall": (_c_int, [_c_int]),
     "muon_ns_normalize": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_normalize_static": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp]),
     "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_f, _vp, _vp]),

@@ -19,6 +19,7 @@
 // parity of `steps` makes the last step write `out`; only in place
 // (out == G) with an odd step count is the result copied once at the end.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -40,6 +41,8 @@ namespace {
 constexpr long long kMaxDim = 1 << 20;
 constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
 constexpr long long kWaitBudgetCycles = 4000000000LL;  // about 2 s at 2 GHz
+std::atomic<long long> g_wait_budget{0};  // 0: kWaitBudgetCycles (muon_ns_set_wait_budget)
+std::atomic<int> g_inject_stall{0};       // muon_ns_inject_stall
 
 struct Problem {
   long long batch, R, C, m, n;
@@ -270,7 +273,8 @@ mns::GemmParams* new_params(int ng, float alpha, float beta, float eps, int* err
   P.beta = beta;
   P.eps = eps;
   P.err = err;
-  P.budget = kWaitBudgetCycles;
+  const long long budget = g_wait_budget.load();
+  P.budget = budget > 0 ? budget : kWaitBudgetCycles;
   return &P;
 }
 
@@ -354,6 +358,8 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
     if (all_have_dep(io, ng)) {
       P->grp[i].dep_wait = io[i].dep;
       P->grp[i].dep_target = static_cast<int>((io[i].step + 1) * dep_per_step_sym(io[i].p));
+      // Injected stall: a target the Gram kernel never reaches.
+      if (io[i].step == 0 && g_inject_stall.load()) P->grp[i].dep_target += 1;
       P->dep_flags = 1;
     }
     if (io[i].half) {
@@ -1117,6 +1123,17 @@ int muon_ns_cached_error(int device, int* device_error) {
   const int s = muon_ns_read_error(ptr, device_error, 0, nullptr);
   cudaSetDevice(prev);
   return s;
+}
+
+int muon_ns_set_wait_budget(long long cycles) {
+  if (cycles < 0) return MUON_NS_ERR_INVALID_ARG;
+  g_wait_budget.store(cycles);
+  return MUON_NS_OK;
+}
+
+int muon_ns_inject_stall(int enable) {
+  g_inject_stall.store(enable != 0 ? 1 : 0);
+  return MUON_NS_OK;
 }
 
 int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols, float eps,

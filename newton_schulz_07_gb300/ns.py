@@ -166,6 +166,19 @@ def read_error(workspace: torch.Tensor, clear: bool = False) -> int:
     return v.value
 
 
+def set_wait_budget(cycles: int) -> None:
+    """Budget of every bounded wait in the kernels, in SM clock cycles (0: the
+    default, about 2 s).  A wait that runs out sets the device error word."""
+    _lib.check(_lib.lib().muon_ns_set_wait_budget(int(cycles)), "muon_ns_set_wait_budget")
+
+
+def inject_stall(enable: bool) -> None:
+    """Host-side fault injection for tests: later whole calls of multi-matrix
+    stacks wait for a completion that never comes, so their bounded waits run
+    out and the device error word is set."""
+    _lib.check(_lib.lib().muon_ns_inject_stall(int(bool(enable))), "muon_ns_inject_stall")
+
+
 def launches_per_call(steps: int) -> int:
     return _lib.lib().muon_ns_launches_per_call(steps)
 

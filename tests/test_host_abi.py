@@ -372,3 +372,13 @@ def test_host_path_argument_errors():
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_host_path_without_device_is_unsupported():
     assert _call_host() == _lib.ERR_UNSUPPORTED_DEVICE
+
+
+def test_wait_budget_and_stall_injection_settings():
+    # Host-side settings only: no device needed.
+    L = _lib.lib()
+    assert L.muon_ns_set_wait_budget(-1) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_set_wait_budget(20_000_000) == _lib.OK
+    assert L.muon_ns_set_wait_budget(0) == _lib.OK
+    assert L.muon_ns_inject_stall(1) == _lib.OK
+    assert L.muon_ns_inject_stall(0) == _lib.OK
