@@ -444,7 +444,7 @@ def main():
             "clocks": clocks,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                     "steps": ne, "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
-                    "largest_chunk_matrices": -(-host_in.shape[0] // 4), "equals_device_result": e2e_same},
+                    "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same},
             "parity": parity,
             "cpu_baseline": cpu,
             "per_shape": per_shape,

@@ -231,10 +231,16 @@ int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, cons
  * largest chunk: when the stack is larger, the first and the last chunk take
  * ceil(chunk / 2) matrices (shorter upload before the first compute and
  * download after the last) and the ones between `chunk`, the one before the
- * last the remainder.  chunk <= 0 selects ceil(batch / 4); chunk > batch is
- * clamped to batch.  Returns MUON_NS_OK or MUON_NS_ERR_INVALID_ARG /
+ * last the remainder.  chunk <= 0 selects the default: the whole stack if it
+ * holds less than 32 MiB, else ceil(96 MiB / (2 * rows * cols)) matrices but
+ * at most ceil(batch / 2).  chunk > batch is clamped to batch.  Returns MUON_NS_OK or MUON_NS_ERR_INVALID_ARG /
  * MUON_NS_ERR_ALIGNMENT as muon_ns_workspace_size(). */
 int muon_ns_host_workspace_size(int batch, int rows, int cols, int chunk, size_t* bytes);
+
+/* Largest chunk, in matrices, that muon_ns_host() uses for this stack and
+ * `chunk` argument (the default rule above for chunk <= 0); 0 for an empty
+ * stack or invalid sizes. */
+int muon_ns_host_chunk(int batch, int rows, int cols, int chunk);
 
 /* out_host = NS(G_host).
  *   G_host, out_host  host, bf16 [batch][rows][cols]; they may be the same

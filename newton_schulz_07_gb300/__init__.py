@@ -17,6 +17,7 @@ from .ns import (  # noqa: F401
     muon_ns_grouped,
     grouped_workspace_size,
     inject_stall,
+    host_chunk,
     host_workspace_size,
     muon_ns_host,
     muon_ns_normalize,

@@ -11,8 +11,10 @@ namespace mns {
 
 // Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel in the stream finishes, and waits for it with
-// griddepcontrol.wait before touching its results.  `cluster_x` > 1 launches
-// clusters of that many CTAs along x.
+// griddepcontrol.wait before touching its results (or, the products of a
+// whole NS call, through per-matrix completion counters, with the wait moved
+// to just before exit).  `cluster_x` > 1 launches clusters of that many CTAs
+// along x.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                cudaStream_t stream, int cluster_x, Args&&... args) {

@@ -22,6 +22,9 @@
 //         every value with j <= i is written to (i, j) and to (j, i), so the
 //         stored matrix is bit-symmetric (one triangle computed and mirrored,
 //         prime-rl PR #3873, Summary item 1; Megatron-LM PR #6381, Summary);
+//         with GemmParams::half_out only inside the diagonal 256 x 256
+//         blocks, the rest of the upper triangle being read transposed by the
+//         consumers (GroupArgs::half_a / half_b);
 //   CL    CTAs per cluster, 1 or 2.  With 2, the two CTAs of a cluster compute
 //         row tiles 2p and 2p + 1 of the same column tile, whose B-operand
 //         panel they share: each loads one half of it with a multicast TMA
@@ -53,10 +56,15 @@
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // main loop of tile t + 1.
 //
-// Every wait on an mbarrier is bounded (clock64 budget).  When one runs out
-// the kernel records MUON_NS_DEVERR_WAIT_TIMEOUT in the error word, every role
-// leaves its loop, the producer waits (bounded) for its copies in flight, the
-// MMA issuer waits (bounded) for its MMAs, and TMEM is freed before return.
+// In a whole NS call the kernel waits, per unit, for the previous product of
+// the same matrix through per-matrix completion counters (GroupArgs::dep_*),
+// and publishes its own units' completion, so consecutive kernels overlap.
+//
+// Every wait on an mbarrier or a counter is bounded (clock64 budget).  When
+// one runs out the kernel records MUON_NS_DEVERR_WAIT_TIMEOUT in the error
+// word, every role leaves its loop, the producer waits (bounded) for its
+// copies in flight, the MMA issuer waits (bounded) for its MMAs, and TMEM is
+// freed before return.
 #pragma once
 
 #include <cstdint>
@@ -217,7 +225,9 @@ constexpr int kDepUnit = 16;
 struct GemmParams {
   CUtensorMap tmA[kMaxGroups];    // A operand (rows of the output)
   CUtensorMap tmB[kMaxGroups];    // B operand (columns of the output)
-  CUtensorMap tmOut[kMaxGroups];  // output, 32 x 32 boxes, 64-byte swizzle
+  // Output in 32-row boxes: 32 x 32 (bf16: 64-byte swizzle; fp32: 128-byte),
+  // or 32 x 64 with the 128-byte swizzle for the 4-warp bf16 update.
+  CUtensorMap tmOut[kMaxGroups];
   // FULL only, optional: the transposed output [batch][N][M] (same boxes),
   // written when out_t != 0.  The fp32 path keeps its iterate in both
   // orientations so that every tensor-core operand is K-major.

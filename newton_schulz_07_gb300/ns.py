@@ -166,6 +166,11 @@ def read_error(workspace: torch.Tensor, clear: bool = False) -> int:
     return v.value
 
 
+def host_chunk(batch: int, rows: int, cols: int, chunk: int = 0) -> int:
+    """Largest chunk (matrices) muon_ns_host uses for this stack and `chunk`."""
+    return _lib.lib().muon_ns_host_chunk(int(batch), int(rows), int(cols), int(chunk))
+
+
 def set_wait_budget(cycles: int) -> None:
     """Budget of every bounded wait in the kernels, in SM clock cycles (0: the
     default, about 2 s).  A wait that runs out sets the device error word."""

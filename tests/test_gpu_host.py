@@ -64,7 +64,7 @@ def test_host_path_expert_stack_vs_device_and_oracle():
     w = ns_inputs.WORKLOADS["experts_16x1536x2048"]
     bits = ns_inputs.stack_bits(w)
     G = host(bits)
-    got = host_bits(ns.muon_ns_host(G))  # default: chunks of 2, 4, 4, 4, 2 matrices
+    got = host_bits(ns.muon_ns_host(G))  # default: chunks of 4, 8, 4 matrices
     np.testing.assert_array_equal(got, device_ref(bits))
     for k in (0, 15):
         ref = oracle.newton_schulz(ns_inputs.bf16_bits_to_f64(bits[k]))

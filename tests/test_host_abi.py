@@ -350,8 +350,18 @@ def test_host_path_workspace_arithmetic():
     for chunk in (1, 3, 16):
         slot = 2 * chunk * 256 * 512 * 2 + ns.workspace_size(chunk, 256, 512)
         assert 2 * slot <= ws(16, 256, 512, chunk) <= 2 * slot + 1024 + 4 * 1024
-    assert ws(16, 256, 512) == ws(16, 256, 512, 4)      # default largest chunk ceil(16 / 4) = 4
-    assert ws(17, 256, 512) == ws(17, 256, 512, 5)      # ceil(17 / 4) = 5
+    # Default largest chunk: the whole stack under 32 MiB ...
+    assert ws(16, 256, 512) == ws(16, 256, 512, 16)
+    # ... else about 96 MiB of input (16 matrices of 1536 x 2048, 4 of 7168 x 2048) ...
+    assert ws(128, 1536, 2048) == ws(128, 1536, 2048, 16)
+    assert ws(32, 7168, 2048) == ws(32, 7168, 2048, 4)
+    # ... but at most half the stack.
+    assert ws(16, 1536, 2048) == ws(16, 1536, 2048, 8)
+    assert ws(17, 1536, 2048) == ws(17, 1536, 2048, 9)
+    assert [ns.host_chunk(*s) for s in [(16, 256, 512), (128, 1536, 2048), (32, 7168, 2048),
+                                        (128, 2048, 768), (16, 1536, 2048), (1, 8192, 8192)]] == [16, 16, 4, 32, 8, 1]
+    assert ns.host_chunk(128, 1536, 2048, 5) == 5 and ns.host_chunk(4, 256, 512, 100) == 4
+    assert ns.host_chunk(0, 256, 512) == 0 and ns.host_chunk(2, 12, 8) == 0
     assert ws(4, 256, 512, 100) == ws(4, 256, 512, 4)   # clamped to the batch
     assert ws(16, 256, 512, 4) > ws(16, 256, 512, 2) > one
     assert ws(0, 256, 512) == 0
