@@ -135,6 +135,34 @@ def test_gram_and_poly_stored_half_in_workspace(shape):
         assert np.linalg.norm(a[k][mask] - x0[mask]) / np.linalg.norm(x0[mask]) < 1.5e-2
 
 
+@pytest.mark.parametrize("shape", [(3, 392, 1000), (2, 1096, 1304), (2, 1304, 1096)])
+def test_call_equals_chain_of_step_calls_bitwise(shape):
+    # A whole call stores A and B half and orders its products per matrix
+    # through completion counters; the per-step entry points store them whole
+    # and wait for whole kernels.  The arithmetic is the same, so are the bits.
+    G = to_dev(random_bits(shape, seed=41))
+    out = ns.muon_ns(G, workspace=ns.alloc_workspace(*shape))
+    ws = ns.alloc_workspace(*shape)
+    ns.muon_ns_normalize(G, ws, norms_only=True)
+    off, nb = ns.workspace_region(*shape, ns._lib.WS_NORMS)
+    norms = ws[off:off + nb].view(torch.float32)
+    b, m = shape[0], min(shape[1:])
+    A = torch.empty((b, m, m), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty_like(A)
+    D = torch.empty((b, m), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, bc, c = ns.DEFAULT_COEFFS
+    X = G
+    for k in range(5):
+        first = norms if k == 0 else None
+        ns.muon_ns_gram(X, A=A, device_error=err, norms=first)
+        ns.muon_ns_poly(A, bc, c, B=B, diag=D, device_error=err)
+        X = ns.muon_ns_update(X, B, a, diag=D, device_error=err, norms=first)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(to_bits(out), to_bits(X))
+
+
 def test_in_place_and_cached_workspace_agree():
     bits = random_bits((3, 136, 264), seed=31)
     ref, _ = run_ws(bits)
