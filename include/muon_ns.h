@@ -149,7 +149,11 @@ int muon_ns_ws(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols
 
 /* As muon_ns_ws() with a workspace cached by the library per device (grown
  * with cudaMalloc when too small, never freed before exit).  Growing is
- * refused with MUON_NS_ERR_WORKSPACE while `stream` is being captured. */
+ * refused with MUON_NS_ERR_WORKSPACE while `stream` is being captured.
+ * Every muon_ns() call on a device shares that workspace, so calls that may
+ * run at the same time on the GPU (different streams) must use muon_ns_ws()
+ * with a workspace each: a shared workspace would mix their iterates and
+ * their per-matrix completion counters. */
 int muon_ns(const muon_bf16* G, muon_bf16* out, int batch, int rows, int cols, int steps,
             const float* coeffs, float eps, cudaStream_t stream);
 
