@@ -477,8 +477,10 @@ struct Stack {
 
 // NS of several stacks, all kernels reporting to `err`.  Stacks are launched
 // together, per orientation, in launches of at most kMaxGroups groups.
+// `cleared`: the caller has already zeroed every stack's tickets and
+// dependency counters.
 int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, int* err, int sms,
-                  cudaStream_t st) {
+                  cudaStream_t st, bool cleared = false) {
   int s = MUON_NS_OK;
   if (steps == 0) {
     for (int i = 0; i < ns; ++i)
@@ -491,8 +493,9 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
   // copy of G is written or read.  One memset clears each stack's norm
   // tickets and its dependency counters.
   for (int i = 0; i < ns; ++i) {
-    if (cudaMemsetAsync(S[i].ws + S[i].L.tickets, 0, 16 * static_cast<size_t>(S[i].p.batch), st) !=
-        cudaSuccess)
+    if (!cleared &&
+        cudaMemsetAsync(S[i].ws + S[i].L.tickets, 0, 16 * static_cast<size_t>(S[i].p.batch), st) !=
+            cudaSuccess)
       return MUON_NS_ERR_CUDA;
     if ((s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st, false)) != MUON_NS_OK)
       return s;
@@ -655,7 +658,12 @@ int run_ns_f32(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* o
 int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, int steps,
            const float abc[3], float eps, uint8_t* ws, int sms, cudaStream_t st) {
   int* err = reinterpret_cast<int*>(ws + L.error);
-  if (cudaMemsetAsync(ws + L.error, 0, 256, st) != cudaSuccess) return MUON_NS_ERR_CUDA;
+  // The error word, the norm tickets and the dependency counters lie end to
+  // end at the start of the workspace: one memset clears them.
+  if (L.error != 0 || L.tickets != 256 || L.deps != L.tickets + 4 * static_cast<size_t>(p.batch))
+    return MUON_NS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, L.deps + 12 * static_cast<size_t>(p.batch), st) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
   Stack S;
   S.p = p;
   S.L = L;
@@ -663,7 +671,7 @@ int run_ns(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* out, 
   S.out = out;
   S.ws = ws;
   S.cur = nullptr;
-  return run_ns_stacks(&S, 1, steps, abc, eps, err, sms, st);
+  return run_ns_stacks(&S, 1, steps, abc, eps, err, sms, st, true);
 }
 
 int check_scalars(int steps, const float* coeffs, float eps, float abc[3]) {
