@@ -925,10 +925,18 @@ namespace {
 // Streams and events of the host-buffer path, created once per device: one
 // stream for uploads, one for downloads; per slot, the events "input
 // uploaded", "chunk computed" and "output downloaded".
+// Chunks in flight in a host-path call: each has its own slot of input,
+// output and NS workspace, so chunk i's upload waits for chunk
+// i - kHostSlots's compute and its compute for that chunk's download.
+#ifndef MNS_HOST_SLOTS
+#define MNS_HOST_SLOTS 2
+#endif
+constexpr int kHostSlots = MNS_HOST_SLOTS;
+
 struct HostPipe {
   bool ready;
   cudaStream_t up, down;
-  cudaEvent_t start, in[2], done[2], out[2];
+  cudaEvent_t start, in[kHostSlots], done[kHostSlots], out[kHostSlots];
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[64];
@@ -941,7 +949,7 @@ int host_pipe_init(HostPipe* hp) {
     cudaGetLastError();
     return MUON_NS_ERR_CUDA;
   }
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < kHostSlots; ++i)
     if (cudaEventCreateWithFlags(&hp->in[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&hp->done[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&hp->out[i], cudaEventDisableTiming) != cudaSuccess) {
@@ -952,10 +960,6 @@ int host_pipe_init(HostPipe* hp) {
   return MUON_NS_OK;
 }
 
-// Largest chunk of a host-path call.  Default ceil(batch / 4): with the
-// half-size first and last chunks below, four full chunks keep each NS call
-// large (few partial waves) while the first upload and the last download,
-// which nothing overlaps, stay at an eighth of the stack each.
 // Largest chunk of a host-path call.  The default takes about 96 MiB of bf16
 // input per chunk, at most half the stack so that copies overlap compute, and
 // the whole stack when it holds less than 32 MiB: every chunk pays a whole
@@ -999,7 +1003,7 @@ HostLayout host_layout(const Problem& pc) {
   H.out = round_up(chunk_bytes, 1024);
   H.ws = H.out + round_up(chunk_bytes, 1024);
   H.slot = round_up(H.ws + make_layout(pc).total, 1024);
-  H.total = 1024 + 2 * H.slot;
+  H.total = 1024 + kHostSlots * H.slot;
   return H;
 }
 
@@ -1073,19 +1077,20 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
     const int nb = host_chunk_size(batch, cb, i);
     if (nb == 0) break;
     nchunks = i + 1;
-    const int sl = i & 1;
+    const int sl = i % kHostSlots;
     const size_t bytes = 2 * mat * nb;
     uint8_t* slot = base + 1024 + sl * H.slot;
     uint16_t* din = reinterpret_cast<uint16_t*>(slot + H.in);
     uint16_t* dout = reinterpret_cast<uint16_t*>(slot + H.out);
-    // Upload once chunk i - 2 has finished reading this slot's input.
-    if (i >= 2 && cudaStreamWaitEvent(hp.up, hp.done[sl], 0) != cudaSuccess) return fail();
+    // Upload once the slot's previous chunk has finished reading its input.
+    if (i >= kHostSlots && cudaStreamWaitEvent(hp.up, hp.done[sl], 0) != cudaSuccess) return fail();
     if (cudaMemcpyAsync(din, G_host + b0 * mat, bytes, cudaMemcpyHostToDevice, hp.up) != cudaSuccess ||
         cudaEventRecord(hp.in[sl], hp.up) != cudaSuccess)
       return fail();
-    // Compute once the input is up and chunk i - 2's output has been downloaded.
+    // Compute once the input is up and the slot's previous output has been
+    // downloaded.
     if (cudaStreamWaitEvent(stream, hp.in[sl], 0) != cudaSuccess) return fail();
-    if (i >= 2 && cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
+    if (i >= kHostSlots && cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
     Problem pi;
     check_shape(nb, rows, cols, &pi, &empty);
     Stack S;
@@ -1105,7 +1110,7 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
     b0 += nb;
   }
   // `stream` completes after the last downloads.
-  for (int sl = 0; sl < 2 && sl < nchunks; ++sl)
+  for (int sl = 0; sl < kHostSlots && sl < nchunks; ++sl)
     if (cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
   return MUON_NS_OK;
 }
