@@ -20,6 +20,7 @@ sample of the same workload (one matrix per step, scaled to a whole call).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -97,7 +98,7 @@ def flop_counts(w, steps=5):
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
@@ -109,12 +110,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
+        """Clock summary of the samples taken inside `window` = (t0, t1) in
+        time.time() seconds (all samples if none falls inside)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -123,25 +126,33 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, mx, reasons, n = [], [], set(), 0
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != len(self.FIELDS):
                 continue
-            n += 1
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            rows.append((ts, parts))
+        inside = [r for r in rows if window and r[0] is not None and window[0] <= r[0] <= window[1]]
+        used = inside if inside else rows
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, parts in used:
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:]):
+            for name, val in zip(names, parts[6:]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": n}
+                "samples": len(used), "window": "timed region" if inside else "whole sampling period"}
 
 
 def gpu_id_for(torch, dev):
@@ -294,6 +305,7 @@ def main():
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     wall0 = time.perf_counter()
+    t_region0 = time.time()
     for i in range(args.steps):
         if scrub is not None:
             scrub.fill_(i & 0xFF)
@@ -302,7 +314,7 @@ def main():
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
+    clocks = sampler.stop(window=(t_region0, time.time()))
     barrier()
     ms_local = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
     ms = max_over_ranks(ms_local)
