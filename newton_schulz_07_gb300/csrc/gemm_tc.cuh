@@ -753,18 +753,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       int ready = 0;
       if (lane == 0)
         ready = detail::wait_bounded<SM2>(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
-      // The previous unit's stores have long completed (this unit's main
-      // loop ran meanwhile): publish it.  The addend, diagonal and norms read
-      // below come from earlier products of matrix b, and the buffers written
-      // below were read by them: the producer's acquire of their counter is
-      // passed on through shared memory.
+      // The addend, diagonal and norms read below come from earlier products
+      // of matrix b, and the buffers written below were read by them: the
+      // producer's acquire of their counter is passed on through shared
+      // memory.
       if (lane == 0 && ready) {
-        if (pend_sig != nullptr) {
-          ptx::bulk_wait_all();
-          ptx::fence_proxy_async_global();
-          ptx::red_release_gpu_add(pend_sig, kSigShare);
-          pend_sig = nullptr;
-        }
         if (G.dep_wait != nullptr &&
             !detail::wait_seen(ptx::smem_u32(&dep_seen_sh), units_done + 1, abort_flag, P.err, P.budget))
           ready = 0;
@@ -825,6 +818,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       auto soff = [](int row, int col) -> uint32_t {
         return F32 ? stage_off32(row, col) : stage_off(row, col);
       };
+      int groups = 0;  // bulk groups this tile has committed (lane 0)
       uint4 av[kAV];
       load_addend(0, av);
 
@@ -937,6 +931,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             if (lane == 0) {
               ptx::tma_store_3d(tmOut, stg, gj0 - h * 32, R0, b);
               ptx::bulk_commit();
+            ++groups;
             }
           }
         } else if (!SYM && P.out_t) {
@@ -953,6 +948,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::tma_store_3d(tmOutT, tr, R0, gj0, b);
             ptx::bulk_commit();
+            ++groups;
           }
         } else if (!SYM) {
           const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kCB);
@@ -962,6 +958,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           if (lane == 0) {
             ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::bulk_commit();
+            ++groups;
           }
         } else if (gj0 < R0 && P.half_out && (gj0 >> 8) != (R0 >> 8)) {
           // Half storage, outside the diagonal 256-block: the chunk alone.
@@ -971,6 +968,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           if (lane == 0) {
             ptx::tma_store_3d(tmOut, stg, gj0, R0, b);
             ptx::bulk_commit();
+            ++groups;
           }
         } else if (gj0 < R0) {
           // Below the diagonal: the chunk at (R0, gj0) and its transpose at (gj0, R0).
@@ -985,6 +983,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::tma_store_3d(tmOut, tr, R0, gj0, b);
             ptx::bulk_commit();
+            ++groups;
           }
         } else {
           // Diagonal 32 x 32 block (gj0 == R0): entry (r, j) takes the value
@@ -1000,6 +999,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           if (lane == 0) {
             ptx::tma_store_3d(tmOut, d, gj0, R0, b);
             ptx::bulk_commit();
+            ++groups;
           }
         }
 #pragma unroll
@@ -1019,7 +1019,20 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       } else {
         ptx::mbar_arrive(sy.tempty(buf));
       }
-      if (lane == 0 && G.dep_sig != nullptr) pend_sig = G.dep_sig + b;
+      if (lane == 0) {
+        // Every tile commits exactly kChunksPerWarp bulk groups (empty ones
+        // pad the chunks it did not store), so once all but the last
+        // kChunksPerWarp have completed, the previous unit's stores, issued a
+        // whole tile ago, have landed: publish that unit now, without waiting
+        // for this unit's stores.
+        for (; groups < kChunksPerWarp; ++groups) ptx::bulk_commit();
+        if (pend_sig != nullptr) {
+          ptx::bulk_wait_complete<kChunksPerWarp>();
+          ptx::fence_proxy_async_global();
+          ptx::red_release_gpu_add(pend_sig, kSigShare);
+        }
+        pend_sig = G.dep_sig != nullptr ? G.dep_sig + b : nullptr;
+      }
       buf ^= 1;
       if (buf == 0) tphase ^= 1u;
     }

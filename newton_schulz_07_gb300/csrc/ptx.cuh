@@ -143,6 +143,13 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Wait until at most N of the most recently committed bulk groups are
+// incomplete (all older groups have completed, writes included).
+template <int N>
+__device__ __forceinline__ void bulk_wait_complete() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Order this thread's async-proxy (TMA) global-memory accesses against its
 // generic-proxy ones: between a completed bulk store and a release that
 // publishes it, and between an acquire and the bulk loads it guards.
