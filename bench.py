@@ -1,18 +1,19 @@
-"""Benchmark of batched quintic Newton–Schulz on one GB300 (or N replicas).
+"""Benchmark of batched quintic Newton–Schulz on one GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--steps K] [--warmup W] [--workload NAME] [--batch B]
                     [--impl ours|reference] [--no-per-shape] [--no-cpu-baseline]
 
-A "step" is one whole NS call (norm, scale, then 5 x Gram / polynomial /
-update) over the workload's stack, inputs resident in HBM.  The default
-workload is the 128-expert MoE stack 128 x 1536 x 2048 (bf16), one of the two
-shapes the method is held to 60% of dense bf16 peak on; every other workload
-is timed briefly under "per_shape".  Rank 0 prints one JSON line.
+A "step" is one whole NS call (norm, then 5 x Gram / polynomial / update)
+over the workload's stack, inputs resident in HBM.  The default workload is
+the 128-expert MoE stack 128 x 1536 x 2048 (bf16), one of the two shapes the
+method is held to 60% of dense bf16 peak on; every other workload is timed
+under "per_shape" (median, min and max of 20 calls each).  One JSON line.
 
-N > 1 (torchrun): each rank runs the same workload on its own GPU with no
-collective in the data path (the NS of a stack does not shard across GPUs
-here: replicas only); a barrier brackets the timed region and the time is the
-maximum over ranks.
+This build is a single-GPU library: its short-contraction products load a
+shared operand panel with TMA multicast inside a cluster of two CTAs, whose
+tensor maps cover only the calling GPU's own buffers, and no data-path step
+exchanges anything between GPUs.  `--impl ours` therefore refuses --gpus > 1
+or WORLD_SIZE > 1 with a one-line error and exit status 2.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (one matrix per step, scaled to a whole call).
@@ -20,6 +21,7 @@ sample of the same workload (one matrix per step, scaled to a whole call).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import datetime
 import hashlib
 import json
@@ -67,18 +69,26 @@ def kernel_source_hash():
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, or None
-    when it is absent or was taken on different kernel sources."""
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu
+    summary, and a note saying where the figure comes from; (None, why) when it
+    is absent or was taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
-        return None
+        return None, "no committed ncu traffic summary"
     if rec.get("source_hash") != kernel_source_hash():
-        return None
+        return None, "kernel sources changed since the committed ncu traffic capture"
     ent = rec.get("kernels", {}).get(workload, {}).get(kernel)
-    return None if ent is None else float(ent["dram_bytes_per_launch"])
+    if ent is None:
+        return None, f"no committed ncu traffic figure for {kernel} on {workload}"
+    note = f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch on {ent['measured_on']}"
+    if ent.get("scale", 1) != 1:
+        note += f", scaled by {ent['scale']:g} (matrices are independent units of a launch)"
+    if "algorithmic_bytes_per_launch" in ent:
+        note += f"; algorithmic bytes per launch {ent['algorithmic_bytes_per_launch']:.4g}"
+    return float(ent["dram_bytes_per_launch"]), note
 
 
 def flop_counts(w, steps=5):
@@ -115,18 +125,17 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self, window=None):
-        """Clock summary of the samples taken inside `window` = (t0, t1) in
-        time.time() seconds (all samples if none falls inside)."""
+    def stop(self):
+        """Stops sampling and keeps the samples as (time.time() seconds, fields)."""
+        self.rows = []
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except Exception:
             self.proc.kill()
             out = ""
-        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != len(self.FIELDS):
@@ -135,8 +144,13 @@ class ClockSampler:
                 ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
             except ValueError:
                 ts = None
-            rows.append((ts, parts))
-        inside = [r for r in rows if window and r[0] is not None and window[0] <= r[0] <= window[1]]
+            self.rows.append((ts, parts))
+
+    def summary(self, window):
+        """Clock summary of the samples taken inside `window` = (t0, t1) in
+        time.time() seconds (all samples if none falls inside)."""
+        rows = getattr(self, "rows", [])
+        inside = [r for r in rows if r[0] is not None and window[0] <= r[0] <= window[1]]
         used = inside if inside else rows
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -241,6 +255,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ns_inputs.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload's shape with this many matrices (small profiling captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-per-shape", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -253,6 +269,11 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if world > 1 or args.gpus > 1:
+        print(f"bench.py: --impl ours runs on one GPU only (got --gpus {args.gpus}, WORLD_SIZE {world}): "
+              "the library's multicast tensor maps cover the calling GPU's own buffers and the path has "
+              "no multi-GPU step", file=sys.stderr, flush=True)
+        return 2
 
     import torch
 
@@ -260,24 +281,10 @@ def main():
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     peaks, peak_src = load_peaks()
     w = ns_inputs.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = dataclasses.replace(w, name=f"{w.name.split('_')[0]}_{args.batch}x{w.rows}x{w.cols}", batch=args.batch)
     fl = flop_counts(w)
 
     bits = ns_inputs.stack_bits(w)
@@ -296,14 +303,13 @@ def main():
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
 
     sampler = ClockSampler(gpu_id_for(torch, dev))
     sampler.start()
     time.sleep(0.3)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
     wall0 = time.perf_counter()
     t_region0 = time.time()
     for i in range(args.steps):
@@ -314,10 +320,9 @@ def main():
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop(window=(t_region0, time.time()))
-    barrier()
-    ms_local = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
-    ms = max_over_ranks(ms_local)
+    t_region1 = time.time()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / args.steps
     dev_err = ns.read_error(ws)
 
     # Per-kernel breakdown: the same kernels in the same launch configuration
@@ -335,6 +340,8 @@ def main():
     n_off, n_bytes = ns.workspace_region(w.batch, w.rows, w.cols, 2)
     norms_t = ws[n_off:n_off + n_bytes].view(torch.float32)
     a, b, c = ns.DEFAULT_COEFFS
+    t_bd0 = time.time()
+    bd_wall0 = time.perf_counter()
     for it in range(nb + 2):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
         ev[0].record(stream)
@@ -358,19 +365,33 @@ def main():
             acc["gram"] += ev[1 + 3 * s].elapsed_time(ev[2 + 3 * s]) / 5
             acc["poly"] += ev[2 + 3 * s].elapsed_time(ev[3 + 3 * s]) / 5
             acc["update"] += ev[3 + 3 * s].elapsed_time(ev[4 + 3 * s]) / 5
+    bd_wall = time.perf_counter() - bd_wall0
+    t_bd1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary((t_region0, t_region1))
+    bd_clocks = sampler.summary((t_bd0, t_bd1))
     per_launch_ms = {k: v / nb for k, v in acc.items()}
     share = {"norm": per_launch_ms["norm"]}
     for k in ("gram", "poly", "update"):
         share[k] = 5 * per_launch_ms[k]
     dominant = max(("gram", "poly", "update"), key=lambda k: share[k])
     achieved = fl[dominant] / (per_launch_ms[dominant] * 1e-3) / 1e12
-    traffic = recorded_traffic(dominant, w.name)
+    # Peak for the roofline: the burst figure when the breakdown loop is short
+    # (under a second) or its sampled SM clock stays within 5 % of the maximum;
+    # the sustained (power-capped) figure otherwise.
+    near_max = bd_clocks is not None and bd_clocks["sm_mhz"] >= 0.95 * bd_clocks["sm_max_mhz"]
+    use_burst = bd_wall < 1.0 or near_max
+    peak = peaks["bf16_tflops"] if use_burst else peaks["bf16_tflops_sustained"]
+    why = (f"breakdown loop {bd_wall:.2f} s" + (" (< 1 s)" if bd_wall < 1.0 else "") +
+           (f", median SM clock {bd_clocks['sm_mhz']:.0f} of {bd_clocks['sm_max_mhz']:.0f} MHz"
+            if bd_clocks else ", no clock samples"))
+    traffic, traffic_note = recorded_traffic(dominant, w.name)
     roofline = {"bound": "tensor", "kernel": f"ns_tc_gemm ({dominant})", "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
-                "traffic": traffic,
+                "frac_of_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peak_src} bf16 {'burst' if use_burst else 'sustained'} ({why})",
+                "traffic": traffic, "traffic_note": traffic_note,
                 "algorithmic_flops_per_launch": fl[dominant],
                 "avg_launch_ms": per_launch_ms[dominant]}
     norm_gbs = fl["norm_bytes"] / (per_launch_ms["norm"] * 1e-3) / 1e9
@@ -380,7 +401,11 @@ def main():
         "norm_hbm": {"achieved_gbs": norm_gbs, "peak_gbs": peaks["hbm_gbs"],
                      "frac": norm_gbs / peaks["hbm_gbs"], "bytes_per_call": fl["norm_bytes"]},
         "tensor_tflops_useful": {k: fl[k] / (per_launch_ms[k] * 1e-3) / 1e12 for k in ("gram", "poly", "update")},
+        "frac_of_peak_useful": {k: fl[k] / (per_launch_ms[k] * 1e-3) / 1e12 / peak for k in ("gram", "poly", "update")},
+        "clocks": bd_clocks,
+        "wall_s": bd_wall,
     }
+    del a_buf, b_buf, x_bufs, d_buf
 
     # End to end through the C ABI with host buffers (muon_ns_host): every step
     # uploads the pinned host stack, orthogonalises it and downloads the
@@ -391,7 +416,6 @@ def main():
     ns.muon_ns_host(host_in, out=host_out, workspace=hws, device=dev)
     torch.cuda.synchronize()
     e2e_same = bool(torch.equal(host_out, out.cpu()))  # the device-resident call's result, bit for bit
-    barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -399,100 +423,111 @@ def main():
         ns.muon_ns_host(host_in, out=host_out, workspace=hws, device=dev, sync=False)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ne)
+    e2e_ms = e0.elapsed_time(e1) / ne
     io_bytes = host_in.numel() * 2
     del hws
 
     # Spot parity of the timed call's output (untimed; matrix 0 vs the oracle).
-    parity = None
-    if rank == 0:
-        import oracle
-        got = ns_inputs.bf16_bits_to_f64(host_out[0].view(torch.int16).numpy().view(np.uint16))
-        ref = oracle.newton_schulz(ns_inputs.bf16_bits_to_f64(bits[0]))
-        parity = {"matrix": 0, "rel_fro_err_vs_fp64_oracle": float(np.linalg.norm(got - ref) / np.linalg.norm(ref)),
-                  "tolerance": 1.5e-2}
+    import oracle
+    got = ns_inputs.bf16_bits_to_f64(host_out[0].view(torch.int16).numpy().view(np.uint16))
+    ref = oracle.newton_schulz(ns_inputs.bf16_bits_to_f64(bits[0]))
+    parity = {"matrix": 0, "rel_fro_err_vs_fp64_oracle": float(np.linalg.norm(got - ref) / np.linalg.norm(ref)),
+              "tolerance": 1.5e-2}
 
     per_shape = None
-    if not args.no_per_shape and world == 1:
+    if not args.no_per_shape:
         per_shape = {}
-        del a_buf, b_buf, x_bufs, d_buf
         for name, ow in ns_inputs.WORKLOADS.items():
             if name == w.name:
                 continue
             per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
         per_shape[w.name + "_fp32_mode"] = time_f32(torch, ns, w, dev, peaks)
-        mixed = [ns_inputs.WORKLOADS["stack_32x7168x2048"], ns_inputs.WORKLOADS["stack_128x2048x768"]]
-        per_shape["mixed_stacks_32x7168x2048+128x2048x768"] = time_grouped(torch, ns, mixed, dev, peaks)
+        for names in (["stack_32x7168x2048", "stack_128x2048x768"],
+                      ["experts_16x1536x2048", "stack_128x2048x768", "tiny_4x256x512"]):
+            per_shape["grouped_" + "+".join(n.split("_", 1)[1] for n in names)] = time_grouped(
+                torch, ns, [ns_inputs.WORKLOADS[n] for n in names], dev, peaks)
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+    cpu = None if args.no_cpu_baseline else cpu_baseline(w)
 
-    if rank == 0:
-        tf_dense = fl["dense_call"] / (ms * 1e-3) / 1e12
-        line = {
-            "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": ms / PAGES_H200_QUACK_MS[w.name] if w.name in PAGES_H200_QUACK_MS else None,
-            "vs_baseline_note": "ms ratio to the pages' H200 QuACK figure for this shape (another GPU; context)",
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "rows": w.rows, "cols": w.cols, "ns_steps": 5,
-                       "coeffs": list(ns.DEFAULT_COEFFS), "eps": ns.DEFAULT_EPS,
-                       "distribution": w.dist, "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": ("flushed between timed steps (256 MiB write)" if flush else
-                              f"working set {working_set / 2**30:.1f} GiB >> L2, no flush")},
-            "tflops_dense_equiv": tf_dense,
-            "tflops_useful": fl["useful_call"] / (ms * 1e-3) / 1e12,
-            "pct_dense_bf16_peak": 100.0 * tf_dense / peaks["bf16_tflops"],
-            "pct_dense_bf16_peak_sustained": 100.0 * tf_dense / peaks["bf16_tflops_sustained"],
-            "peak_source": peak_src,
-            "aggregate_calls_per_s": world * 1e3 / ms,
-            "gpu_launches": args.steps * ns.launches_per_call(5),
-            "launches_per_step": ns.launches_per_call(5),
-            "wall_s_timed": wall,
-            "device_error_word": dev_err,
-            "roofline": roofline,
-            "breakdown": breakdown,
-            "clocks": clocks,
-            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
-                    "steps": ne, "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
-                    "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same},
-            "parity": parity,
-            "cpu_baseline": cpu,
-            "per_shape": per_shape,
-            "kernel_source_hash": kernel_source_hash(),
-        }
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    tf_dense = fl["dense_call"] / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": ms / PAGES_H200_QUACK_MS[w.name] if w.name in PAGES_H200_QUACK_MS else None,
+        "vs_baseline_note": "ms ratio to the pages' H200 QuACK figure for this shape (another GPU; context)",
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "rows": w.rows, "cols": w.cols, "ns_steps": 5,
+                   "coeffs": list(ns.DEFAULT_COEFFS), "eps": ns.DEFAULT_EPS,
+                   "distribution": w.dist, "parallelism": "single GPU",
+                   "l2": ("flushed between timed steps (256 MiB write)" if flush else
+                          f"working set {working_set / 2**30:.1f} GiB >> L2, no flush")},
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "tflops_dense_equiv": tf_dense,
+        "tflops_useful": fl["useful_call"] / (ms * 1e-3) / 1e12,
+        "pct_dense_bf16_peak": 100.0 * tf_dense / peaks["bf16_tflops"],
+        "pct_dense_bf16_peak_sustained": 100.0 * tf_dense / peaks["bf16_tflops_sustained"],
+        "peak_source": peak_src,
+        "gpu_launches": args.steps * ns.launches_per_call(5),
+        "launches_per_step": ns.launches_per_call(5),
+        "wall_s_timed": wall,
+        "device_error_word": dev_err,
+        "roofline": roofline,
+        "breakdown": breakdown,
+        "clocks": clocks,
+        "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+                "steps": ne, "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
+                "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same},
+        "parity": parity,
+        "cpu_baseline": cpu,
+        "per_shape": per_shape,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
-def time_workload(torch, ns, w, dev, peaks, steps=10, warmup=3):
+def time_calls(torch, fns, stream, calls=20, warmup=3, scrub=None):
+    """Times each function of `fns` (a dict name -> callable), one call of each
+    per round, `calls` rounds, with CUDA events on `stream` around each call and
+    L2 flushed before it.  Returns name -> {median, min, max, mean, calls} in ms."""
+    for fn in fns.values():
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    ms = {k: [] for k in fns}
+    for i in range(calls):
+        for k, fn in fns.items():
+            if scrub is not None:
+                scrub.fill_(i & 0xFF)
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            ms[k].append(s.elapsed_time(e))
+    return {k: {"median": statistics.median(v), "min": min(v), "max": max(v), "mean": sum(v) / len(v),
+                "calls": len(v)} for k, v in ms.items()}
+
+
+def rates(w_dense, w_useful, ms, peaks):
+    tf = w_dense / (ms * 1e-3) / 1e12
+    return {"tflops_dense_equiv": tf, "tflops_useful": w_useful / (ms * 1e-3) / 1e12,
+            "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"]}
+
+
+def time_workload(torch, ns, w, dev, peaks, calls=20, warmup=3):
+    """Whole muon_ns_ws calls on workload w: median, min and max of `calls`."""
     bits = ns_inputs.stack_bits(w)
     G = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
     out = torch.empty_like(G)
     ws = ns.alloc_workspace(w.batch, w.rows, w.cols, device=dev)
     scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        ns.muon_ns(G, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(dev)
-    tot = 0.0
-    for i in range(steps):
-        scrub.fill_(i & 0xFF)
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        ns.muon_ns(G, out=out, workspace=ws)
-        e.record(stream)
-        torch.cuda.synchronize()
-        tot += s.elapsed_time(e)
-    ms = tot / steps
-    tf = w.dense_flops() / (ms * 1e-3) / 1e12
-    res = {"ms": ms, "tflops_dense_equiv": tf, "tflops_useful": w.useful_flops() / (ms * 1e-3) / 1e12,
-           "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"], "batch": w.batch, "rows": w.rows,
-           "cols": w.cols, "steps": steps, "l2": "flushed between timed steps",
+    t = time_calls(torch, {"call": lambda: ns.muon_ns(G, out=out, workspace=ws)},
+                   torch.cuda.current_stream(dev), calls, warmup, scrub)["call"]
+    res = {"ms": t["median"], "ms_min": t["min"], "ms_max": t["max"], "ms_mean": t["mean"], "calls": t["calls"],
+           **rates(w.dense_flops(), w.useful_flops(), t["median"], peaks),
+           "batch": w.batch, "rows": w.rows, "cols": w.cols, "l2": "flushed before each timed call",
            "device_error_word": ns.read_error(ws)}
     if w.name in PAGES_H200_QUACK_MS:
         res["pages_h200_quack_ms"] = PAGES_H200_QUACK_MS[w.name]
@@ -501,40 +536,32 @@ def time_workload(torch, ns, w, dev, peaks, steps=10, warmup=3):
     return res
 
 
-def time_f32(torch, ns, w, dev, peaks, steps=10, warmup=3):
+def time_f32(torch, ns, w, dev, peaks, calls=20, warmup=3):
     """The fp32 NS mode (tf32 tensor cores, fp32 storage) on workload w, with
     matrix 0's error against the fp64 oracle."""
     x = np.stack([ns_inputs.matrix_f32(w, k) for k in range(w.batch)])
     G = torch.from_numpy(x).to(dev)
     out = torch.empty_like(G)
     ws = torch.empty(ns.f32_workspace_size(w.batch, w.rows, w.cols), dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        ns.muon_ns_f32(G, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(dev)
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        ns.muon_ns_f32(G, out=out, workspace=ws)
-    e.record(stream)
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    t = time_calls(torch, {"call": lambda: ns.muon_ns_f32(G, out=out, workspace=ws)},
+                   torch.cuda.current_stream(dev), calls, warmup)["call"]
     import oracle
     ref = oracle.newton_schulz(x[0].astype(np.float64))
     err = float(np.linalg.norm(out[0].double().cpu().numpy() - ref) / np.linalg.norm(ref))
-    tf = w.dense_flops() / (ms * 1e-3) / 1e12
-    res = {"ms": ms, "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
+    tf = w.dense_flops() / (t["median"] * 1e-3) / 1e12
+    res = {"ms": t["median"], "ms_min": t["min"], "ms_max": t["max"], "calls": t["calls"],
+           "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
            "mode": "fp32 in/out, tf32 tensor cores", "rel_fro_err_matrix0_vs_fp64_oracle": err,
-           "steps": steps, "l2": f"working set >> L2 ({w.name})", "device_error_word": ns.read_error(ws)}
+           "l2": f"working set >> L2 ({w.name})", "device_error_word": ns.read_error(ws)}
     del G, out, ws
     torch.cuda.empty_cache()
     return res
 
 
-def time_grouped(torch, ns, wls, dev, peaks, steps=10, warmup=3):
+def time_grouped(torch, ns, wls, dev, peaks, calls=20, warmup=3):
     """One muon_ns_grouped call over several stacks (one optimizer step's NS
-    over parameter groups of different shapes)."""
+    over parameter groups of different shapes) against the same stacks as
+    back-to-back muon_ns_ws calls, interleaved call by call."""
     Gs = [torch.from_numpy(ns_inputs.stack_bits(w).view(np.int16)).view(torch.bfloat16).to(dev) for w in wls]
     outs = [torch.empty_like(G) for G in Gs]
     ws = torch.empty(ns.grouped_workspace_size(Gs), dtype=torch.uint8, device=dev)
@@ -544,36 +571,19 @@ def time_grouped(torch, ns, wls, dev, peaks, steps=10, warmup=3):
     def grouped():
         ns.muon_ns_grouped(Gs, outs=outs, workspace=ws)
 
-    def separate():  # the same stacks as back-to-back muon_ns_ws calls
-        for G, o, w in zip(Gs, outs, sws):
-            ns.muon_ns(G, out=o, workspace=w)
+    def separate():
+        for G, o, wsi in zip(Gs, outs, sws):
+            ns.muon_ns(G, out=o, workspace=wsi)
 
-    stream = torch.cuda.current_stream(dev)
-
-    def timed(fn):
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            scrub.fill_(i & 0xFF)
-            s = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            fn()
-            e.record(stream)
-            torch.cuda.synchronize()
-            tot += s.elapsed_time(e)
-        return tot / steps
-
-    sep_ms = timed(separate)
-    ms = timed(grouped)
-    dense = sum(w.dense_flops() for w in wls)
-    tf = dense / (ms * 1e-3) / 1e12
-    res = {"ms": ms, "tflops_dense_equiv": tf, "pct_dense_bf16_peak": 100 * tf / peaks["bf16_tflops"],
-           "stacks": [w.name for w in wls], "api": "muon_ns_grouped (one call)", "steps": steps,
-           "separate_calls_ms": sep_ms,
-           "l2": "flushed between timed steps", "device_error_word": ns.read_error(ws)}
+    t = time_calls(torch, {"separate": separate, "grouped": grouped}, torch.cuda.current_stream(dev),
+                   calls, warmup, scrub)
+    g, sp = t["grouped"], t["separate"]
+    res = {"ms": g["median"], "ms_min": g["min"], "ms_max": g["max"], "calls": g["calls"],
+           **rates(sum(w.dense_flops() for w in wls), sum(w.useful_flops() for w in wls), g["median"], peaks),
+           "stacks": [w.name for w in wls], "api": "muon_ns_grouped (one call)",
+           "separate_calls_ms": sp["median"], "separate_calls_ms_min": sp["min"], "separate_calls_ms_max": sp["max"],
+           "grouped_over_separate": g["median"] / sp["median"],
+           "l2": "flushed before each timed call", "device_error_word": ns.read_error(ws)}
     if all(w.name in PAGES_H200_QUACK_MS for w in wls):
         res["pages_h200_quack_ms_sum"] = sum(PAGES_H200_QUACK_MS[w.name] for w in wls)
     del Gs, outs, ws, sws, scrub

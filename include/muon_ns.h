@@ -50,7 +50,13 @@
  *     before anything is launched; a non-OK status means nothing was enqueued
  *     (except MUON_NS_ERR_CUDA, which reports a failed launch).
  *   - Only GPUs of compute capability 10.3 (sm_103) are supported; others get
- *     MUON_NS_ERR_UNSUPPORTED_DEVICE.
+ *     MUON_NS_ERR_UNSUPPORTED_DEVICE.  The kernels are built for sm_103a
+ *     alone (tcgen05, TMA), so no other device could run them.
+ *   - One GPU per process.  Products with contractions up to 1024 run on
+ *     pairs of CTAs that load a shared operand panel with TMA multicast within
+ *     their cluster; every tensor map covers only buffers on the calling GPU,
+ *     and nothing in the library exchanges data between GPUs.  Processes that
+ *     drive more than one GPU are not a supported use.
  *   - Limits: batch, rows, cols <= 1<<20 and each matrix below 2^31 elements.
  *   - Errors found on the device (a bounded wait inside a kernel that ran out)
  *     set a device error word; the call that launched the kernels cannot
@@ -267,6 +273,25 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
  * MUON_NS_ERR_TIMEOUT if the word is nonzero, else MUON_NS_OK or an error. */
 int muon_ns_read_error(const void* workspace, int* device_error, int clear, cudaStream_t stream);
 
+/* Asynchronous check of a call's device error word: enqueues on `stream` one
+ * copy of the first int of `workspace` (a muon_ns_ws(), muon_ns_grouped() or
+ * muon_ns_host() workspace) into *host_word and returns without
+ * synchronising or allocating, so the check can follow a call inside a
+ * captured CUDA graph and is replayed with it.
+ *   host_word  page-locked (cudaHostAlloc, cudaHostRegister, a pinned torch
+ *              tensor) or managed memory, owned by the caller; pageable memory
+ *              is rejected with MUON_NS_ERR_INVALID_ARG, since its copy would
+ *              synchronise.
+ * Read *host_word once the stream has passed the copy (synchronise the stream
+ * or an event recorded after this call): 0 = no kernel reported an error;
+ * MUON_NS_DEVERR_WAIT_TIMEOUT set = a bounded wait ran out, i.e. the call's
+ * status is MUON_NS_ERR_TIMEOUT.  The next whole call on the workspace clears
+ * the word.  Returns MUON_NS_OK, MUON_NS_ERR_INVALID_ARG (NULL or pageable
+ * pointer), MUON_NS_ERR_ALIGNMENT (workspace not 256-byte aligned) or
+ * MUON_NS_ERR_CUDA (the copy could not be enqueued).  This is the
+ * asynchronous counterpart of muon_ns_read_error(), which synchronises. */
+int muon_ns_check(const void* workspace, int* host_word, cudaStream_t stream);
+
 /* Same for the workspace cached by muon_ns() on `device` (synchronises the
  * device).  *device_error = 0 if no cached workspace exists yet. */
 int muon_ns_cached_error(int device, int* device_error);
@@ -355,7 +380,11 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, mu
  *   - Every call shares the one array; it keeps the last call's contents and
  *     the call zeroes what must start at zero.  Calls that overlap on the GPU
  *     (different streams, no ordering) race on it and give wrong results.
- *   - Other arguments, errors and aliasing as for muon_ns_normalize(). */
+ *   - X must not be NULL (MUON_NS_ERR_INVALID_ARG): the norms stay in the
+ *     library's private array, where the caller cannot read them, so a
+ *     norms-only call would have no result.
+ *   - Other arguments, errors and aliasing (X == G allowed) as for
+ *     muon_ns_normalize(). */
 int muon_ns_normalize_static(const muon_bf16* G, muon_bf16* X, int batch, int rows, int cols,
                              float eps, cudaStream_t stream);
 

@@ -8,8 +8,10 @@ from .ns import (  # noqa: F401
     DEFAULT_COEFFS,
     DEFAULT_EPS,
     alloc_workspace,
+    error_status,
     launches_per_call,
     muon_ns,
+    muon_ns_check,
     muon_ns_f32,
     f32_workspace_region,
     f32_workspace_size,

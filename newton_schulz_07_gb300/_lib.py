@@ -19,6 +19,8 @@ ERR_WORKSPACE = 4
 ERR_CUDA = 5
 ERR_TIMEOUT = 6
 
+DEVERR_WAIT_TIMEOUT = 1  # bit of the device error word
+
 WS_TOTAL, WS_ERROR, WS_NORMS, WS_X, WS_GRAM, WS_POLY, WS_DIAG = range(7)
 
 _c_int, _c_ll, _c_sz, _c_f, _vp = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
@@ -52,6 +54,7 @@ SIGNATURES = {
     "muon_ns_host_chunk": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "muon_ns_host": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _c_int, _vp, _c_sz, _vp]),
     "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),
+    "muon_ns_check": (_c_int, [_vp, _vp, _vp]),
     "muon_ns_cached_error": (_c_int, [_c_int, _pi]),
     "muon_ns_set_wait_budget": (_c_int, [_c_ll]),
     "muon_ns_inject_stall": (_c_int, [_c_int]),

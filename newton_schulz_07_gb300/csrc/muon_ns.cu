@@ -1135,6 +1135,25 @@ int muon_ns_read_error(const void* workspace, int* device_error, int clear, cuda
   return v ? MUON_NS_ERR_TIMEOUT : MUON_NS_OK;
 }
 
+int muon_ns_check(const void* workspace, int* host_word, cudaStream_t stream) {
+  if (!workspace || !host_word) return MUON_NS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  // The word must be memory the copy engine writes without staging
+  // (page-locked or registered host memory, or managed memory): a pageable
+  // destination would make the copy synchronous and cannot be captured.
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host_word) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_INVALID_ARG;
+  }
+  if (a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged) return MUON_NS_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(host_word, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_NS_ERR_CUDA;
+  }
+  return MUON_NS_OK;
+}
+
 int muon_ns_cached_error(int device, int* device_error) {
   if (!device_error || device < 0 || device >= 64) return MUON_NS_ERR_INVALID_ARG;
   void* ptr;

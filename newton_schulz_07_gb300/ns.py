@@ -166,6 +166,24 @@ def read_error(workspace: torch.Tensor, clear: bool = False) -> int:
     return v.value
 
 
+def muon_ns_check(workspace: torch.Tensor, host_word: torch.Tensor) -> None:
+    """Enqueue on the current stream a copy of the workspace's device error
+    word into `host_word` (a pinned host int32 tensor of one element); no
+    synchronisation, so it can be captured in a CUDA graph.  After the stream
+    passes the copy, error_status(host_word.item()) gives the call's status."""
+    if (not isinstance(host_word, torch.Tensor) or host_word.dtype != torch.int32 or host_word.is_cuda
+            or host_word.numel() < 1 or not host_word.is_pinned()):
+        raise TypeError("host_word must be a pinned host int32 tensor")
+    with torch.cuda.device(workspace.device):
+        _lib.check(_lib.lib().muon_ns_check(_ptr(workspace), _ptr(host_word), _stream(workspace.device)),
+                   "muon_ns_check")
+
+
+def error_status(word: int) -> int:
+    """Status of a call from its device error word (see muon_ns_check)."""
+    return _lib.ERR_TIMEOUT if int(word) & _lib.DEVERR_WAIT_TIMEOUT else _lib.OK
+
+
 def host_chunk(batch: int, rows: int, cols: int, chunk: int = 0) -> int:
     """Largest chunk (matrices) muon_ns_host uses for this stack and `chunk`."""
     return _lib.lib().muon_ns_host_chunk(int(batch), int(rows), int(cols), int(chunk))

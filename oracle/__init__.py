@@ -15,7 +15,5 @@ from .ns_fp64 import (  # noqa: F401
     newton_schulz_trace,
     normalize,
     poly,
-    quintic,
-    quintic_composed,
     update,
 )

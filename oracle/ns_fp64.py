@@ -57,8 +57,6 @@ __all__ = [
     "newton_schulz",
     "newton_schulz_trace",
     "newton_schulz_batched",
-    "quintic",
-    "quintic_composed",
 ]
 
 
@@ -141,17 +139,3 @@ def newton_schulz_batched(G: np.ndarray, steps: int = DEFAULT_STEPS, coeffs=DEFA
         out[k] = newton_schulz_trace(G[k], steps, coeffs, eps)["out"]
     return out
 
-
-def quintic(s, coeffs=DEFAULT_COEFFS):
-    """p(s) = a s + b s^3 + c s^5: what one NS step does to each singular value."""
-    a, b, c = (float(v) for v in coeffs)
-    s = np.asarray(s, dtype=np.float64)
-    return a * s + b * s ** 3 + c * s ** 5
-
-
-def quintic_composed(s, steps: int = DEFAULT_STEPS, coeffs=DEFAULT_COEFFS):
-    """p applied `steps` times (composition, not a power)."""
-    s = np.asarray(s, dtype=np.float64)
-    for _ in range(int(steps)):
-        s = quintic(s, coeffs)
-    return s

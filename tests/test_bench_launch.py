@@ -32,3 +32,16 @@ def test_reference_arm_single_process():
     assert p.returncode == 0, p.stderr[-2000:]
     d = json.loads(p.stdout.strip().splitlines()[-1])
     assert d["cpu_baseline"]["cores"] >= 1 and d["metric"].startswith("ms per NS call")
+
+
+def test_cuda_arm_refuses_more_than_one_gpu():
+    # The library is for 1-GPU processes (its multicast tensor maps cover the
+    # calling GPU's own buffers): bench.py --impl ours stops before touching a
+    # GPU, whether N comes from --gpus or from a launcher's WORLD_SIZE.
+    script = os.path.join(ROOT, "bench.py")
+    for extra, env in ((["--gpus", "2"], {}), ([], {"WORLD_SIZE": "2", "RANK": "1"})):
+        p = subprocess.run([sys.executable, script, "--steps", "3", "--warmup", "3"] + extra,
+                           stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=120, cwd=ROOT,
+                           env=dict(os.environ, **env))
+        assert p.returncode == 2, p.stderr
+        assert "one GPU only" in p.stderr and p.stdout.strip() == ""

@@ -153,14 +153,6 @@ def test_orthogonal_invariance():
     assert rel_err(oracle.newton_schulz(Q @ G @ P), Q @ oracle.newton_schulz(G) @ P) < 1e-12
 
 
-def test_quintic_values():
-    # p(1) = a + b + c, p(0) = 0, p is odd.
-    assert abs(oracle.quintic(1.0) - (3.4445 - 4.7750 + 2.0315)) < 1e-15
-    assert oracle.quintic(0.0) == 0.0
-    assert oracle.quintic(-0.3) == -oracle.quintic(0.3)
-    assert abs(oracle.quintic_composed(0.5, 2) - oracle.quintic(oracle.quintic(0.5))) < 1e-15
-
-
 # ---------------------------------------------------------------------------
 # Planted mistakes: each must make at least one pin fail.
 # ---------------------------------------------------------------------------

@@ -19,6 +19,8 @@ import pytest
 import torch
 
 import newton_schulz_07_gb300 as ns
+import ns_inputs
+import oracle
 from newton_schulz_07_gb300 import _lib
 from nsutil import random_bits, to_bits, to_dev, to_f64
 
@@ -46,6 +48,11 @@ def test_static_scratch_matches_workspace_entry_point_two_calls(shape):
         assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
         # Same kernels, same fixed reduction order: identical bits.
         np.testing.assert_array_equal(to_bits(X_static), to_bits(X_ref))
+        # And against the definition, G / (||G||_F + eps) in fp64: one bf16
+        # rounding (2^-8 relative) on top of an fp32 norm (1e-4 is ample).
+        g = ns_inputs.bf16_bits_to_f64(bits)
+        exact = np.stack([oracle.normalize(g[k], 1e-7) for k in range(shape[0])])
+        assert np.all(np.abs(got - exact) <= (2.0 ** -8 + 1e-4) * np.abs(exact) + 1e-30)
 
 
 def test_static_scratch_rejects_problems_beyond_its_size():
@@ -58,3 +65,12 @@ def test_static_scratch_rejects_problems_beyond_its_size():
     s = _lib.lib().muon_ns_normalize_static(ctypes.c_void_p(G.data_ptr()), ctypes.c_void_p(G.data_ptr()), b, r, c,
                                             ctypes.c_float(1e-7), None)
     assert s == _lib.ERR_WORKSPACE
+
+
+def test_static_scratch_rejects_a_null_output():
+    # Its norms stay in the library's private array, so a call without X
+    # would compute nothing the caller can read: rejected before any launch.
+    G = torch.empty((2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    s = _lib.lib().muon_ns_normalize_static(ctypes.c_void_p(G.data_ptr()), None, 2, 64, 128,
+                                            ctypes.c_float(1e-7), None)
+    assert s == _lib.ERR_INVALID_ARG
