@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for batched quintic Newton–Schulz.
+"""fp64 CPU oracle for batched quintic Newton–Schulz and the Muon step around it.
 
 TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
 benchmark's CPU-baseline / reference leg, never by the product library.  It
@@ -16,4 +16,12 @@ from .ns_fp64 import (  # noqa: F401
     normalize,
     poly,
     update,
+)
+from .muon_step import (  # noqa: F401
+    apply_update,
+    default_scale,
+    momentum_update,
+    muon_step,
+    ns_input,
+    round_bf16,
 )
