@@ -442,6 +442,7 @@ def main():
                 continue
             per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
         per_shape[w.name + "_fp32_mode"] = time_f32(torch, ns, w, dev, peaks)
+        per_shape["muon_step_" + w.name.split("_", 1)[1]] = time_muon_step(torch, ns, w, dev, peaks)
         for names in (["stack_32x7168x2048", "stack_128x2048x768"],
                       ["experts_16x1536x2048", "stack_128x2048x768", "tiny_4x256x512"]):
             per_shape["grouped_" + "+".join(n.split("_", 1)[1] for n in names)] = time_grouped(
@@ -587,6 +588,65 @@ def time_grouped(torch, ns, wls, dev, peaks, calls=20, warmup=3):
     if all(w.name in PAGES_H200_QUACK_MS for w in wls):
         res["pages_h200_quack_ms_sum"] = sum(PAGES_H200_QUACK_MS[w.name] for w in wls)
     del Gs, outs, ws, sws, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_muon_step(torch, ns, w, dev, peaks, calls=20, warmup=3):
+    """The Muon step around NS on workload w's shape: fp32 masters W, momentum
+    M and gradient G (G from the workload's distribution), one fused
+    muon_step_ws call against the chain muon_momentum -> muon_ns_ws ->
+    muon_apply, interleaved call by call; plus the momentum kernel alone
+    (HBM-bound) and matrix 0 against the fp64 oracle step."""
+    lr, mu, wd = 0.02, 0.95, 0.01
+    G = torch.from_numpy(np.stack([ns_inputs.matrix_f32(w, k) for k in range(w.batch)])).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(1234)
+    W = torch.randn(G.shape, generator=gen, device=dev) * 0.02
+    M = torch.randn(G.shape, generator=gen, device=dev) * 0.02
+    W0, M0 = W[0].cpu().numpy(), M[0].cpu().numpy()
+    sws = torch.empty(ns.step_workspace_size(w.batch, w.rows, w.cols), dtype=torch.uint8, device=dev)
+    ws1, ws2 = ns.alloc_workspace(w.batch, w.rows, w.cols, device=dev), ns.alloc_workspace(w.batch, w.rows, w.cols, device=dev)
+    U = torch.empty(G.shape, dtype=torch.bfloat16, device=dev)
+    O = torch.empty_like(U)
+    # Parity of one fused step on matrix 0 (untimed, before W and M move on).
+    ns.muon_step(W, M, G, lr, momentum=mu, weight_decay=wd, workspace=sws)
+    torch.cuda.synchronize()
+    import oracle
+    W_ref, M_ref, O_ref = oracle.muon_step(W0, M0, G[0].cpu().numpy(), lr, mu, weight_decay=wd)
+    upd = lr * ns.default_scale(w.rows, w.cols) * np.linalg.norm(O_ref)
+    parity = {"matrix": 0, "w_update_rel_err_vs_fp64_oracle": float(np.linalg.norm(W[0].cpu().numpy() - W_ref) / upd),
+              "m_max_abs_err": float(np.max(np.abs(M[0].cpu().numpy() - M_ref))), "tolerance": 1.5e-2}
+
+    def fused():
+        ns.muon_step(W, M, G, lr, momentum=mu, weight_decay=wd, workspace=sws)
+
+    def chain():
+        ns.muon_momentum(M, G, ws1, momentum=mu, U=U)
+        ns.muon_ns(U, out=O, workspace=ws2)
+        ns.muon_apply(W, O, lr, weight_decay=wd)
+
+    def momentum_only():
+        ns.muon_momentum(M, G, ws1, momentum=mu, U=U)
+
+    stream = torch.cuda.current_stream(dev)
+    t = time_calls(torch, {"fused": fused, "chain": chain, "momentum": momentum_only}, stream, calls, warmup)
+    f, c, mo = t["fused"], t["chain"], t["momentum"]
+    mom_bytes = w.batch * w.rows * w.cols * (4 + 4 + 4 + 2)  # read G, M; write M, U
+    res = {"ms": f["median"], "ms_min": f["min"], "ms_max": f["max"], "calls": f["calls"],
+           **rates(w.dense_flops(), w.useful_flops(), f["median"], peaks),
+           "api": "muon_step_ws (one call: momentum + norm, NS, update fused into the last product)",
+           "launches": ns.step_launches(5),
+           "chain_ms": c["median"], "chain_ms_min": c["min"],
+           "chain_api": "muon_momentum -> muon_ns_ws -> muon_apply (separate passes)",
+           "fused_over_chain": f["median"] / c["median"],
+           "momentum_kernel": {"ms": mo["median"], "bytes": mom_bytes,
+                               "gbs": mom_bytes / (mo["median"] * 1e-3) / 1e9,
+                               "frac_of_hbm_peak": mom_bytes / (mo["median"] * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+           "hparams": {"lr": lr, "momentum": mu, "nesterov": True, "weight_decay": wd,
+                       "scale": ns.default_scale(w.rows, w.cols)},
+           "parity": parity, "device_error_word": ns.read_error(sws),
+           "l2": "working set >> L2"}
+    del G, W, M, sws, ws1, ws2, U, O
     torch.cuda.empty_cache()
     return res
 

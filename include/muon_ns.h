@@ -389,6 +389,66 @@ int muon_ns_normalize_static(const muon_bf16* G, muon_bf16* X, int batch, int ro
                              float eps, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The Muon optimizer step around NS.  prime-rl PR #3873 (Summary) speeds up
+ * "the Muon optimizer step" whose inner loop is the NS above; param-decomp PR
+ * #978 (What, `ns_dtype`) runs that NS in bf16 while "masters/momentum stay
+ * fp32".  The pages print no formula for the step; the one taken here, per
+ * matrix W (fp32 master), G (fp32 gradient), M (fp32 momentum buffer), is
+ *
+ *   M' = mu M + G
+ *   U  = G + mu M'   (nesterov != 0)      or   U = M'   (nesterov == 0)
+ *   O  = NS(bf16(U))                      (the bf16 NS of muon_ns_ws)
+ *   W' = (1 - lr wd) W - lr scale O
+ *
+ * in fp32 (fused multiply-adds), with U rounded once to bf16 (nearest, ties
+ * to even).  `scale` is the caller's shape factor on the update; the Python
+ * binding defaults it to sqrt(max(1, rows / cols)).  W, M and G are device
+ * fp32 [batch][rows][cols], contiguous, 16-byte aligned and pairwise
+ * disjoint; the shape rules are those of muon_ns_ws.
+ * ------------------------------------------------------------------------- */
+
+typedef struct {
+  float lr;            /* learning rate */
+  float momentum;      /* mu */
+  float weight_decay;  /* decoupled: W <- (1 - lr weight_decay) W - ... */
+  float scale;         /* factor on the orthogonalised update */
+  int nesterov;        /* nonzero: U = G + mu M'; zero: U = M' */
+} muon_step_hparams;
+
+/* Workspace bytes of muon_step_ws(): the muon_ns_ws() workspace of the stack
+ * (same regions, muon_ns_workspace_region) followed by the bf16 U. */
+int muon_step_workspace_size(int batch, int rows, int cols, size_t* bytes);
+
+/* One Muon step of a stack, in place on W and M, G read only.  Kernel
+ * launches: 1 + 3 * steps (3 if steps == 0).  The first kernel does the
+ * momentum update, writes U and computes ||U||_F (the same fp32 value the NS
+ * norm kernel would compute on U), so the NS needs no norm pass; the last
+ * update product writes W' directly instead of storing O, so neither O nor
+ * a separate update pass exists.  Results equal muon_momentum() ->
+ * muon_ns_ws() on U -> muon_apply() bit for bit.  Hyperparameters must be
+ * finite (MUON_NS_ERR_INVALID_ARG); the other arguments, errors and the
+ * device error word (first int of the workspace) are as for muon_ns_ws().
+ * Nothing is allocated and nothing synchronises. */
+int muon_step_ws(float* W, float* M, const float* G, int batch, int rows, int cols,
+                 const muon_step_hparams* hp, int steps, const float* coeffs, float eps, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
+/* The step's first kernel alone: M = mu M + G in place, U = bf16 NS input
+ * (device bf16 [batch][rows][cols]), and ||U||_F into the MUON_NS_WS_NORMS
+ * region of `workspace` (a muon_ns_ws() workspace of the stack).  M and G
+ * must not overlap. */
+int muon_momentum(float* M, const float* G, muon_bf16* U, int batch, int rows, int cols, float momentum,
+                  int nesterov, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The step's update alone: W = (1 - lr wd) W - lr scale O for a device bf16 O
+ * of W's shape (the NS output); hp->momentum and hp->nesterov are unused. */
+int muon_apply(float* W, const muon_bf16* O, int batch, int rows, int cols, const muon_step_hparams* hp,
+               cudaStream_t stream);
+
+/* Kernel launches of one muon_step_ws() call: 1 + 3 * steps (3 if steps == 0). */
+int muon_step_launches(int steps);
+
+/* ---------------------------------------------------------------------------
  * Host-only helpers (no GPU needed).
  * ------------------------------------------------------------------------- */
 

@@ -8,6 +8,7 @@ from .ns import (  # noqa: F401
     DEFAULT_COEFFS,
     DEFAULT_EPS,
     alloc_workspace,
+    default_scale,
     error_status,
     launches_per_call,
     muon_ns,
@@ -26,8 +27,13 @@ from .ns import (  # noqa: F401
     muon_ns_normalize_static,
     muon_ns_poly,
     muon_ns_update,
+    muon_apply,
+    muon_momentum,
+    muon_step,
     read_error,
     set_wait_budget,
+    step_launches,
+    step_workspace_size,
     workspace_region,
     workspace_size,
 )

@@ -36,6 +36,15 @@ class MuonNSStack(ctypes.Structure):
 
 _pst = ctypes.POINTER(MuonNSStack)
 
+
+class MuonStepHparams(ctypes.Structure):
+    """muon_step_hparams of include/muon_ns.h."""
+    _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("scale", ctypes.c_float), ("nesterov", ctypes.c_int)]
+
+
+_php = ctypes.POINTER(MuonStepHparams)
+
 # name -> (restype, argtypes); the exported C ABI, in header order.
 SIGNATURES = {
     "muon_ns_version": (ctypes.c_char_p, []),
@@ -63,6 +72,11 @@ SIGNATURES = {
     "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_f, _vp, _vp]),
     "muon_ns_poly": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
     "muon_ns_update": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_f, _vp, _vp]),
+    "muon_step_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _psz]),
+    "muon_step_ws": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _php, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
+    "muon_momentum": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _vp]),
+    "muon_apply": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _php, _vp]),
+    "muon_step_launches": (_c_int, [_c_int]),
     "muon_ns_launches_per_call": (_c_int, [_c_int]),
     "muon_ns_tile_count": (_c_ll, [_c_int, _c_int, _c_int, _c_int]),
     "muon_ns_tile_coords": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_ll, _pi, _pi, _pi]),

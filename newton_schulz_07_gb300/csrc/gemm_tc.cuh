@@ -216,6 +216,12 @@ struct GroupArgs {
   int* dep_sig;
   const int* dep_wait;
   int dep_target;
+  // Last update of a Muon step (FULL bf16 products only, optional): instead
+  // of storing the iterate, each output value o, rounded to bf16 as it would
+  // be stored, updates the fp32 master in place,
+  //   w_out[b][i][j] = w_decay * w_out[b][i][j] - w_lrs * o,
+  // with w_out laid out like the output ([batch][M][N], row stride ld).
+  float* w_out;
 };
 
 // Counter increment per finished unit of the tile space, whatever the
@@ -250,6 +256,7 @@ struct GemmParams {
   // the previous grid only before it exits, so that its completion still
   // implies that of every earlier kernel in the stream.
   int dep_flags;
+  float w_decay, w_lrs;  // GroupArgs::w_out: 1 - lr wd and lr scale
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -476,6 +483,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // transposed (num_kb: never), as in the MMA issuer.
         const int kb_a = G.half_a ? min(256 * ((I >> 1) + 1) / EC::kBlockK, num_kb) : num_kb;
         const int kb_b = G.half_b ? min(256 * (J + 1) / EC::kBlockK, num_kb) : num_kb;
+        // Diagonal unit of a symmetric product on a CTA pair: the B panel is
+        // the pair's own two A tiles (rows 256 J .. 256 J + 255), so each CTA
+        // loads its row tile once and both operands are read from it.
+        const bool diag = SYM && CL == 2 && J == (I >> 1);
         // The operands of matrix b are complete once the previous product
         // has finished all of its units.  Every unit is then counted for the
         // epilogue, which reads the same inputs' addend and diagonal.
@@ -508,9 +519,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             if (SM2) {
               // This CTA's A tile and its half of the B panel, into its own
               // shared memory; all bytes of the pair are counted on CTA 0's
-              // barrier, which expects both CTAs' stages.
+              // barrier, which expects both CTAs' stages.  On a diagonal unit
+              // the A tile is also this CTA's half of the panel.
               const uint32_t fb = ptx::mapa(sy.full(stage), 0);
-              if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), 2 * R::kStageBytes);
+              if (leader) ptx::mbar_arrive_expect_tx(sy.full(stage), diag ? 2 * kABytes : 2 * R::kStageBytes);
               if (AMN) {
 #pragma unroll
                 for (int c = 0; c < kTileM / EC::kMnChunk; ++c)
@@ -518,13 +530,30 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               } else {
                 ptx::tma_load_3d_pair(sa, mA, fb, k0, row0, b);
               }
-              if (BMN) {
+              if (diag) {
+              } else if (BMN) {
 #pragma unroll
                 for (int c = 0; c < kNch / 2; ++c)
                   ptx::tma_load_3d_pair(sb + c * EC::kMnChunkBytes, mB, fb,
                                         col0 + (static_cast<int>(crank) * (kNch / 2) + c) * EC::kMnChunk, k0, b);
               } else {
                 ptx::tma_load_3d_pair(sb, mB, fb, k0, col0 + static_cast<int>(crank) * (kTileN / 2), b);
+              }
+            } else if (CL == 2 && diag) {
+              // Multicast pair, diagonal unit: each CTA's half of the shared
+              // panel is its own A tile, so only the panel is loaded and the A
+              // operand is read from this CTA's half of it.
+              ptx::mbar_arrive_expect_tx(sy.full(stage), kBBytes);
+              if (BMN) {
+#pragma unroll
+                for (int c = 0; c < kNch / 2; ++c) {
+                  const int cg = static_cast<int>(crank) * (kNch / 2) + c;
+                  ptx::tma_load_3d_mc(sb + cg * EC::kMnChunkBytes, mB, sy.full(stage),
+                                      col0 + cg * EC::kMnChunk, k0, b, 0x3);
+                }
+              } else {
+                ptx::tma_load_3d_mc(sb + crank * (kBBytes / 2), mB, sy.full(stage), k0,
+                                    col0 + static_cast<int>(crank) * (kTileN / 2), b, 0x3);
               }
             } else {
               ptx::mbar_arrive_expect_tx(sy.full(stage), R::kStageBytes);
@@ -621,12 +650,18 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // MMA shares N between the pair's row tiles and always takes 256.
         bool half_n = false;
         int tI = 0, tJ = 0;
-        if ((SYM && !SM2) || G.half_a || G.half_b) {
+        if (SYM || G.half_a || G.half_b) {
           int b;
           tile_decode(G.space, t - G.tile_begin, &b, &tI, &tJ);
           tI = row_tile(tI);
           half_n = SYM && !SM2 && (tI & 1) == 0 && tJ == (tI >> 1);
         }
+        // Diagonal unit of a pair (as in the producer): one copy of each row
+        // tile serves as both operands.  2-SM MMAs read the B panel halves
+        // from the A tiles; multicast pairs read A from this CTA's panel half.
+        const bool diag = SYM && CL == 2 && tJ == (tI >> 1);
+        const uint32_t a_off = (diag && !SM2) ? static_cast<uint32_t>(kABytes + crank * (kBBytes / 2)) : 0u;
+        const uint32_t b_off = (diag && SM2) ? 0u : static_cast<uint32_t>(kABytes);
         // k-block from which an operand of a half-stored matrix is read
         // transposed (num_kb: never).
         const int kb_a = G.half_a ? min(256 * ((tI >> 1) + 1) / EC::kBlockK, num_kb) : num_kb;
@@ -653,8 +688,8 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               return;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = smem_base + stage * R::kStageBytes;
-            const uint32_t sb = sa + kABytes;
+            const uint32_t sa = smem_base + stage * R::kStageBytes + a_off;
+            const uint32_t sb = smem_base + stage * R::kStageBytes + b_off;
 #pragma unroll
             for (int kk = 0; kk < EC::kBlockK / EC::kMmaK; ++kk) {
               // K-major: an MMA's K slice is 32 bytes further along the swizzle
@@ -877,6 +912,32 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             }
           }
           G.diag_out[static_cast<long long>(b) * G.M + gi] = dval;
+        }
+        if (!SYM && !F32 && G.w_out != nullptr) {
+          // Muon step: the master weights take this chunk's values in place
+          // of the stored iterate (16-byte loads and stores of this lane's
+          // row; N is a multiple of 8, so a 4-column group is wholly in or out).
+          if (row_ok) {
+            float* wr = G.w_out + static_cast<long long>(b) * G.bstride + gi * G.ld + gj0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (gj0 + 4 * g + 4 > G.N) break;
+              const uint4 wv = ptx::ld_global_v4(reinterpret_cast<const uint4*>(wr + 4 * g));
+              const uint32_t lo = detail::pack_bf16x2(f[4 * g], f[4 * g + 1]);
+              const uint32_t hi = detail::pack_bf16x2(f[4 * g + 2], f[4 * g + 3]);
+              const float o[4] = {detail::bf16_lo(lo), detail::bf16_hi(lo), detail::bf16_lo(hi), detail::bf16_hi(hi)};
+              const float w[4] = {__uint_as_float(wv.x), __uint_as_float(wv.y), __uint_as_float(wv.z),
+                                  __uint_as_float(wv.w)};
+              ptx::st_global_v4(reinterpret_cast<uint4*>(wr + 4 * g),
+                                __float_as_uint(fmaf(-P.w_lrs, o[0], P.w_decay * w[0])),
+                                __float_as_uint(fmaf(-P.w_lrs, o[1], P.w_decay * w[1])),
+                                __float_as_uint(fmaf(-P.w_lrs, o[2], P.w_decay * w[2])),
+                                __float_as_uint(fmaf(-P.w_lrs, o[3], P.w_decay * w[3])));
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < kAV; ++g) av[g] = an[g];
+          continue;
         }
         // Output words: 32 fp32 (rounded to tf32 when they feed an MMA) or 16
         // pairs of bf16; ew(j) is element j as raw bits.

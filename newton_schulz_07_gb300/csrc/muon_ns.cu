@@ -33,6 +33,7 @@
 #include "gemm_launch.cuh"
 #include "gemm_tc.cuh"
 #include "internal.h"
+#include "muon_step.cuh"
 #include "norm.cuh"
 
 namespace {
@@ -232,6 +233,11 @@ struct StepIO {
   // instead of for the whole previous kernel.
   int* dep;
   int step;
+  // Update only, optional: the last update of a Muon step updates these fp32
+  // master weights ([batch][rows][cols]) in place of storing Xn:
+  // W = w_decay W - w_lrs bf16(Xn).
+  float* W;
+  float w_decay, w_lrs;
 };
 
 // Counter value per matrix after one step of a product: its units per matrix
@@ -415,6 +421,12 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     P->grp[i].addend = io[i].X;
     P->grp[i].diag_in = io[i].D;
     P->grp[i].norms = io[i].norms;
+    if (io[i].W != nullptr) {
+      if (f32) return MUON_NS_ERR_INVALID_ARG;  // the Muon step runs the bf16 NS
+      P->grp[i].w_out = io[i].W;
+      P->w_decay = io[i].w_decay;
+      P->w_lrs = io[i].w_lrs;
+    }
     // Signals the update counter; waits for this step's polynomial.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + 2 * p.batch;
     if (all_have_dep(io, ng)) {
@@ -473,14 +485,19 @@ struct Stack {
   uint16_t* out;
   uint8_t* ws;  // this stack's workspace (layout L)
   uint16_t* cur;
+  // Muon step, optional: the last update writes W = w_decay W - w_lrs NS(G)
+  // (fp32 masters) instead of `out`, which then holds no result.
+  float* W = nullptr;
+  float w_decay = 1.0f, w_lrs = 0.0f;
 };
 
 // NS of several stacks, all kernels reporting to `err`.  Stacks are launched
 // together, per orientation, in launches of at most kMaxGroups groups.
 // `cleared`: the caller has already zeroed every stack's tickets and
-// dependency counters.
+// dependency counters.  `norms_ready`: the caller has already written every
+// stack's norms of G (the Muon step's momentum kernel), so no norm kernel runs.
 int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, int* err, int sms,
-                  cudaStream_t st, bool cleared = false) {
+                  cudaStream_t st, bool cleared = false, bool norms_ready = false) {
   int s = MUON_NS_OK;
   if (steps == 0) {
     for (int i = 0; i < ns; ++i)
@@ -497,7 +514,8 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
         cudaMemsetAsync(S[i].ws + S[i].L.tickets, 0, 16 * static_cast<size_t>(S[i].p.batch), st) !=
             cudaSuccess)
       return MUON_NS_ERR_CUDA;
-    if ((s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st, false)) != MUON_NS_OK)
+    if (!norms_ready &&
+        (s = run_normalize(S[i].p, S[i].L, S[i].G, nullptr, eps, S[i].ws, st, false)) != MUON_NS_OK)
       return s;
   }
   StepIO io[mns::kMaxGroups];
@@ -528,6 +546,13 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
           e.D = reinterpret_cast<float*>(t.ws + t.L.diag);
           e.norms = (k == 0) ? reinterpret_cast<const float*>(t.ws + t.L.norms) : nullptr;
           e.Xn = nxt;
+          if (t.W != nullptr && k + 1 == steps) {
+            // The Muon step's last update writes the masters; Xn only
+            // names a valid buffer for the output tensor map.
+            e.W = t.W;
+            e.w_decay = t.w_decay;
+            e.w_lrs = t.w_lrs;
+          }
           e.half = MNS_HALF_SYM && !t.p.f32;
           e.step = k;
           // A single matrix gains nothing (its next product needs all of
@@ -573,7 +598,7 @@ int run_ns_stacks(Stack* S, int ns, int steps, const float abc[3], float eps, in
     }
   }
   for (int i = 0; i < ns; ++i)
-    if (S[i].cur != S[i].out &&
+    if (S[i].W == nullptr && S[i].cur != S[i].out &&
         cudaMemcpyAsync(S[i].out, S[i].cur, S[i].L.x_bytes, cudaMemcpyDeviceToDevice, st) !=
             cudaSuccess)
       return MUON_NS_ERR_CUDA;
@@ -1267,6 +1292,163 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, mu
   io.Xn = Xn;
   return run_update(&io, 1, a, eps, false, device_error, d.sms, stream);
 }
+
+}  // extern "C"
+
+// ------------------------------------------------------------- Muon step --
+
+namespace {
+
+// decay = 1 - lr wd and lrs = lr scale, in fp32, from finite hyperparameters.
+int check_hparams(const muon_step_hparams* hp, float* decay, float* lrs) {
+  if (!hp) return MUON_NS_ERR_INVALID_ARG;
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->momentum) || !std::isfinite(hp->weight_decay) ||
+      !std::isfinite(hp->scale))
+    return MUON_NS_ERR_INVALID_ARG;
+  *decay = 1.0f - hp->lr * hp->weight_decay;
+  *lrs = hp->lr * hp->scale;
+  return MUON_NS_OK;
+}
+
+// A Muon-step workspace is the NS workspace of the stack followed by the
+// bf16 NS input U [batch][rows][cols].
+size_t step_u_offset(const Layout& L) { return round_up(L.total, 1024); }
+size_t step_ws_total(const Problem& p, const Layout& L) {
+  return step_u_offset(L) + round_up(2 * static_cast<size_t>(p.batch) * p.R * p.C, 1024);
+}
+
+// The momentum kernel over the stack; tickets must be zero (it writes the
+// norms of U into the workspace's norm region).
+int launch_momentum(const Problem& p, const Layout& L, const float* G, float* M, uint16_t* U, float mu,
+                    int nesterov, uint8_t* ws, cudaStream_t st) {
+  const long long vec = p.R * p.C / 8;
+  const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
+  return to_status(mns::launch_pdl(mns::muon_momentum_norm, grid, dim3(mns::kNormThreads), 0, st,
+                                   reinterpret_cast<const float4*>(G), reinterpret_cast<float4*>(M),
+                                   reinterpret_cast<uint4*>(U), vec, L.chunks, mu, nesterov ? 1 : 0,
+                                   reinterpret_cast<float*>(ws + L.partials),
+                                   reinterpret_cast<unsigned int*>(ws + L.tickets),
+                                   reinterpret_cast<float*>(ws + L.norms)));
+}
+
+// W = decay W - lrs O over n elements (a multiple of 8), grid-stride with at
+// most 8 CTAs of 256 threads per SM.
+int launch_apply(float* W, const uint16_t* O, long long n, float decay, float lrs, int sms, cudaStream_t st) {
+  const long long n8 = n / 8;
+  const long long want = (n8 + 255) / 256;
+  const long long cap = 8LL * sms;
+  const unsigned blocks = static_cast<unsigned>(std::max(1LL, std::min(want, cap)));
+  return to_status(mns::launch_pdl(mns::muon_apply, dim3(blocks), dim3(256), 0, st, reinterpret_cast<float4*>(W),
+                                   reinterpret_cast<const uint4*>(O), n8, decay, lrs));
+}
+
+bool overlap(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int muon_step_workspace_size(int batch, int rows, int cols, size_t* bytes) {
+  if (!bytes) return MUON_NS_ERR_INVALID_ARG;
+  Problem p;
+  bool empty;
+  const int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  *bytes = empty ? 0 : step_ws_total(p, make_layout(p));
+  return MUON_NS_OK;
+}
+
+int muon_step_ws(float* W, float* M, const float* G, int batch, int rows, int cols,
+                 const muon_step_hparams* hp, int steps, const float* coeffs, float eps, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  float abc[3], decay, lrs;
+  if ((s = check_scalars(steps, coeffs, eps, abc)) != MUON_NS_OK) return s;
+  if ((s = check_hparams(hp, &decay, &lrs)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!W || !M || !G) return MUON_NS_ERR_INVALID_ARG;
+  const size_t fbytes = 4 * static_cast<size_t>(p.batch) * p.R * p.C;
+  if (overlap(W, M, fbytes) || overlap(W, G, fbytes) || overlap(M, G, fbytes)) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(M) || !aligned16(G)) return MUON_NS_ERR_ALIGNMENT;
+  const Layout L = make_layout(p);
+  if (!workspace || workspace_bytes < step_ws_total(p, L)) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* U = reinterpret_cast<uint16_t*>(ws + step_u_offset(L));
+  // Error word, norm tickets and dependency counters in one memset.
+  if (cudaMemsetAsync(ws, 0, L.deps + 12 * static_cast<size_t>(p.batch), stream) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
+  if ((s = launch_momentum(p, L, G, M, U, hp->momentum, hp->nesterov, ws, stream)) != MUON_NS_OK) return s;
+  if (steps == 0) {
+    // O = U / (||U||_F + eps) into the iterate region, then the update.
+    uint16_t* O = reinterpret_cast<uint16_t*>(ws + L.x);
+    const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
+    if (mns::launch_pdl(mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, stream,
+                        reinterpret_cast<const uint4*>(U), reinterpret_cast<uint4*>(O), p.R * p.C / 8,
+                        reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
+      return MUON_NS_ERR_CUDA;
+    return launch_apply(W, O, p.batch * p.R * p.C, decay, lrs, d.sms, stream);
+  }
+  Stack S;
+  S.p = p;
+  S.L = L;
+  S.G = U;
+  S.out = U;  // in place: U is dead once step 1 has read it
+  S.ws = ws;
+  S.cur = nullptr;
+  S.W = W;
+  S.w_decay = decay;
+  S.w_lrs = lrs;
+  return run_ns_stacks(&S, 1, steps, abc, eps, reinterpret_cast<int*>(ws + L.error), d.sms, stream, true, true);
+}
+
+int muon_momentum(float* M, const float* G, muon_bf16* U, int batch, int rows, int cols, float momentum,
+                  int nesterov, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  if (!std::isfinite(momentum)) return MUON_NS_ERR_INVALID_ARG;
+  if (empty) return MUON_NS_OK;
+  if (!M || !G || !U) return MUON_NS_ERR_INVALID_ARG;
+  if (overlap(M, G, 4 * static_cast<size_t>(p.batch) * p.R * p.C)) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(M) || !aligned16(G) || !aligned16(U)) return MUON_NS_ERR_ALIGNMENT;
+  const Layout L = make_layout(p);
+  if (!workspace || workspace_bytes < L.total) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), stream) != cudaSuccess)
+    return MUON_NS_ERR_CUDA;
+  return launch_momentum(p, L, G, M, U, momentum, nesterov, ws, stream);
+}
+
+int muon_apply(float* W, const muon_bf16* O, int batch, int rows, int cols, const muon_step_hparams* hp,
+               cudaStream_t stream) {
+  Problem p;
+  bool empty;
+  int s = check_shape(batch, rows, cols, &p, &empty);
+  if (s != MUON_NS_OK) return s;
+  float decay, lrs;
+  if ((s = check_hparams(hp, &decay, &lrs)) != MUON_NS_OK) return s;
+  if (empty) return MUON_NS_OK;
+  if (!W || !O) return MUON_NS_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(O)) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  return launch_apply(W, O, p.batch * p.R * p.C, decay, lrs, d.sms, stream);
+}
+
+int muon_step_launches(int steps) { return steps < 0 ? -1 : (steps == 0 ? 3 : 1 + 3 * steps); }
 
 int muon_ns_launches_per_call(int steps) {
   return steps < 0 ? -1 : (steps == 0 ? 2 : 1 + 3 * steps);

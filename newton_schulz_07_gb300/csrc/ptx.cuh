@@ -172,6 +172,10 @@ __device__ __forceinline__ float ld_global_f32(const float* p) {
   asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
+// Plain 16-byte store to the global space.
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 // Release store and acquire load of a shared-memory word at CTA scope.
 __device__ __forceinline__ void st_release_cta_shared(uint32_t addr, int v) {

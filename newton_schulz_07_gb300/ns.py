@@ -6,6 +6,7 @@ device memory and the current stream.  Names follow the C entry points.
 from __future__ import annotations
 
 import ctypes
+import math
 
 import torch
 
@@ -326,3 +327,77 @@ def muon_ns_host(G: torch.Tensor, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: fl
         if sync:
             torch.cuda.current_stream(dev).synchronize()
     return out
+
+
+# ---------------------------------------------------------------- Muon step --
+
+def _check_f32(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
+
+
+def default_scale(rows: int, cols: int) -> float:
+    """sqrt(max(1, rows / cols)): the shape factor on the orthogonalised update."""
+    return math.sqrt(max(1.0, rows / cols))
+
+
+def _hparams(lr, momentum, weight_decay, scale, nesterov):
+    return _lib.MuonStepHparams(float(lr), float(momentum), float(weight_decay), float(scale), int(bool(nesterov)))
+
+
+def step_workspace_size(batch: int, rows: int, cols: int) -> int:
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_step_workspace_size(batch, rows, cols, ctypes.byref(n)), "muon_step_workspace_size")
+    return n.value
+
+
+def muon_step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, lr: float, momentum: float = 0.95,
+              nesterov: bool = True, weight_decay: float = 0.0, scale: float | None = None, steps: int = 5,
+              coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS, workspace: torch.Tensor | None = None) -> None:
+    """One Muon step, in place on the fp32 master W and momentum M, for an
+    fp32 gradient G (matrix or (batch, rows, cols) stack):
+    M = mu M + G; U = G + mu M (Nesterov) or M; W = (1 - lr wd) W - lr scale NS(bf16(U)).
+    `scale` defaults to sqrt(max(1, rows / cols))."""
+    for t, n in ((W, "W"), (M, "M"), (G, "G")):
+        _check_f32(t, n)
+        if t.shape != W.shape or t.device != W.device:
+            raise ValueError("W, M and G must have one shape and device")
+    b, r, c = _shape3(W)
+    hp = _hparams(lr, momentum, weight_decay, default_scale(r, c) if scale is None else scale, nesterov)
+    if workspace is None:
+        workspace = torch.empty(max(step_workspace_size(b, r, c), 1), dtype=torch.uint8, device=W.device)
+    with torch.cuda.device(W.device):
+        _lib.check(_lib.lib().muon_step_ws(_ptr(W), _ptr(M), _ptr(G), b, r, c, ctypes.byref(hp), int(steps),
+                                           _coeffs(coeffs), float(eps), _ptr(workspace), workspace.numel(),
+                                           _stream(W.device)), "muon_step_ws")
+
+
+def muon_momentum(M: torch.Tensor, G: torch.Tensor, workspace: torch.Tensor, momentum: float = 0.95,
+                  nesterov: bool = True, U: torch.Tensor | None = None) -> torch.Tensor:
+    """The step's first kernel: M = mu M + G in place; returns the bf16 NS
+    input U; ||U||_F goes to the (muon_ns_ws) workspace's NORMS region."""
+    _check_f32(M, "M")
+    _check_f32(G, "G")
+    b, r, c = _shape3(M)
+    U = torch.empty(M.shape, dtype=torch.bfloat16, device=M.device) if U is None else U
+    _check_bf16(U, "U")
+    with torch.cuda.device(M.device):
+        _lib.check(_lib.lib().muon_momentum(_ptr(M), _ptr(G), _ptr(U), b, r, c, float(momentum), int(bool(nesterov)),
+                                            _ptr(workspace), workspace.numel(), _stream(M.device)), "muon_momentum")
+    return U
+
+
+def muon_apply(W: torch.Tensor, O: torch.Tensor, lr: float, weight_decay: float = 0.0,
+               scale: float | None = None) -> None:
+    """The step's update alone: W = (1 - lr wd) W - lr scale O (O bf16, W's shape)."""
+    _check_f32(W, "W")
+    _check_bf16(O, "O")
+    b, r, c = _shape3(W)
+    hp = _hparams(lr, 0.0, weight_decay, default_scale(r, c) if scale is None else scale, False)
+    with torch.cuda.device(W.device):
+        _lib.check(_lib.lib().muon_apply(_ptr(W), _ptr(O), b, r, c, ctypes.byref(hp), _stream(W.device)),
+                   "muon_apply")
+
+
+def step_launches(steps: int) -> int:
+    return _lib.lib().muon_step_launches(steps)

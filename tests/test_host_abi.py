@@ -26,7 +26,7 @@ TILE_M, TILE_N = 128, 256
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(muon_ns\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(muon_\w+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_function():
