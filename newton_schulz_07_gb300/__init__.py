@@ -21,6 +21,7 @@ from .ns import (  # noqa: F401
     grouped_workspace_size,
     inject_stall,
     host_chunk,
+    host_plan,
     host_workspace_size,
     muon_ns_host,
     muon_ns_normalize,

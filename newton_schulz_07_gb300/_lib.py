@@ -61,6 +61,7 @@ SIGNATURES = {
     "muon_ns_grouped": (_c_int, [_pst, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_ns_host_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _psz]),
     "muon_ns_host_chunk": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
+    "muon_ns_host_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int]),
     "muon_ns_host": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _pf, _c_f, _c_int, _vp, _c_sz, _vp]),
     "muon_ns_read_error": (_c_int, [_vp, _pi, _c_int, _vp]),
     "muon_ns_check": (_c_int, [_vp, _vp, _vp]),

@@ -49,11 +49,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // unit of the tile space.  Clusters are further limited to the number that
 // can be resident at once (the kernel is persistent).
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32 = false, int CL = 1,
-          bool SM2 = false>
+          bool SM2 = false, bool WOUT = false>
 cudaError_t launch_tc_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Smem<SYM, EPI_WARPS, F32, SM2>::kSmemBytes;
   constexpr int kThreads = Epi<EPI_WARPS>::kCtaThreads;
-  auto kernel = ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS, F32, CL, SM2>;
+  auto kernel = ns_tc_gemm<A_MN, B_MN, SYM, EPI_WARPS, F32, CL, SM2, WOUT>;
   // Set up once per device: the dynamic shared-memory limit, and for
   // clusters the number of clusters that fit on the GPU at once.
   static std::atomic<unsigned long long> configured{0};

@@ -30,6 +30,9 @@
 //         panel they share: each loads one half of it with a multicast TMA
 //         copy into both CTAs' shared memory, and each MMA commit releases the
 //         stage in both CTAs.  Half the B-operand bytes per CTA come from L2;
+//   WOUT  (update products only) the last update of a Muon step: the
+//         epilogue updates the fp32 master weights in place of storing the
+//         iterate (GroupArgs::w_out), prefetching their rows one chunk ahead;
 //   SM2   (CL == 2 only) the pair runs 2-SM MMAs instead: one thread of CTA 0
 //         issues M = 256 tcgen05.mma.cta_group::2 over A tiles held by both
 //         CTAs (128 rows each) and a B panel split in halves between them,
@@ -83,6 +86,12 @@ constexpr int kABytes = kTileM * 128;          // A tile: 128 rows of 128 bytes 
 constexpr int kBBytes = kTileN * 128;          // B panel: 256 rows of 128 bytes (32 KB)
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
+// Diagonal units of symmetric products on CTA pairs load each row tile once
+// (it is both the A tile and a half of the B panel); MNS_DIAG_ONCE=0 loads
+// both operands as on every other unit.
+#ifndef MNS_DIAG_ONCE
+#define MNS_DIAG_ONCE 1
+#endif
 
 
 // Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
@@ -370,11 +379,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, bool SM2 = false>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, bool SM2 = false, bool WOUT = false>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   static_assert(!SM2 || CL == 2, "2-SM MMAs run on CTA pairs");
+  static_assert(!WOUT || (!SYM && !F32), "master-weight output: bf16 update products only");
   using EC = ElemCfg<F32>;
   using R = Smem<SYM, EPI_WARPS, F32, SM2>;
   extern __shared__ uint8_t smem_raw[];
@@ -486,7 +496,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // Diagonal unit of a symmetric product on a CTA pair: the B panel is
         // the pair's own two A tiles (rows 256 J .. 256 J + 255), so each CTA
         // loads its row tile once and both operands are read from it.
-        const bool diag = SYM && CL == 2 && J == (I >> 1);
+        const bool diag = MNS_DIAG_ONCE && SYM && CL == 2 && J == (I >> 1);
         // The operands of matrix b are complete once the previous product
         // has finished all of its units.  Every unit is then counted for the
         // epilogue, which reads the same inputs' addend and diagonal.
@@ -659,7 +669,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         // Diagonal unit of a pair (as in the producer): one copy of each row
         // tile serves as both operands.  2-SM MMAs read the B panel halves
         // from the A tiles; multicast pairs read A from this CTA's panel half.
-        const bool diag = SYM && CL == 2 && tJ == (tI >> 1);
+        const bool diag = MNS_DIAG_ONCE && SYM && CL == 2 && tJ == (tI >> 1);
         const uint32_t a_off = (diag && !SM2) ? static_cast<uint32_t>(kABytes + crank * (kBBytes / 2)) : 0u;
         const uint32_t b_off = (diag && SM2) ? 0u : static_cast<uint32_t>(kABytes);
         // k-block from which an operand of a half-stored matrix is read
@@ -785,6 +795,25 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       // A row tile past the last one (second CTA of a cluster, odd row-tile
       // count) was computed on zero-filled operands: nothing to store.
       const int n_chunks = (CL == 2 && I * kTileM >= G.M) ? 0 : kChunksPerWarp;
+      // Muon step (GroupArgs::w_out): this lane's row of the master weights,
+      // 32 fp32 columns per chunk, is loaded one chunk ahead; chunk 0 before
+      // the accumulator wait, which hides its latency.  W is written by no
+      // other kernel of the call, so it may be read early.
+      constexpr bool kW = WOUT;
+      const bool wmode = kW && G.w_out != nullptr;
+      float* wrow = nullptr;
+      uint4 wv[kW ? 8 : 1];
+      auto load_w = [&](int cc, uint4 (&dst)[kW ? 8 : 1]) {
+        const int gj0 = J * kTileN + (c_begin + cc) * 32;
+#pragma unroll
+        for (int g = 0; g < (kW ? 8 : 1); ++g)
+          if (wrow != nullptr && gj0 + 4 * g + 4 <= G.N) dst[g] = ptx::ld_global_v4(wrow + gj0 + 4 * g);
+      };
+      if (wmode) {
+        const long long wi = static_cast<long long>(I) * kTileM + r_in_tile;
+        if (wi < G.M && n_chunks > 0) wrow = G.w_out + static_cast<long long>(b) * G.bstride + wi * G.ld;
+        load_w(0, wv);
+      }
       int ready = 0;
       if (lane == 0)
         ready = detail::wait_bounded<SM2>(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
@@ -913,28 +942,30 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           }
           G.diag_out[static_cast<long long>(b) * G.M + gi] = dval;
         }
-        if (!SYM && !F32 && G.w_out != nullptr) {
+        if (wmode) {
           // Muon step: the master weights take this chunk's values in place
-          // of the stored iterate (16-byte loads and stores of this lane's
-          // row; N is a multiple of 8, so a 4-column group is wholly in or out).
-          if (row_ok) {
-            float* wr = G.w_out + static_cast<long long>(b) * G.bstride + gi * G.ld + gj0;
+          // of the stored iterate, w = w_decay w - w_lrs bf16(f) (16-byte
+          // loads and stores of this lane's row; N is a multiple of 8, so a
+          // 4-column group is wholly in or out).
+          uint4 wn[kW ? 8 : 1];
+          if (cc + 1 < n_chunks) load_w(cc + 1, wn);
+          if (wrow != nullptr) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
+            for (int g = 0; g < (kW ? 8 : 1); ++g) {
               if (gj0 + 4 * g + 4 > G.N) break;
-              const uint4 wv = ptx::ld_global_v4(reinterpret_cast<const uint4*>(wr + 4 * g));
               const uint32_t lo = detail::pack_bf16x2(f[4 * g], f[4 * g + 1]);
               const uint32_t hi = detail::pack_bf16x2(f[4 * g + 2], f[4 * g + 3]);
               const float o[4] = {detail::bf16_lo(lo), detail::bf16_hi(lo), detail::bf16_lo(hi), detail::bf16_hi(hi)};
-              const float w[4] = {__uint_as_float(wv.x), __uint_as_float(wv.y), __uint_as_float(wv.z),
-                                  __uint_as_float(wv.w)};
-              ptx::st_global_v4(reinterpret_cast<uint4*>(wr + 4 * g),
-                                __float_as_uint(fmaf(-P.w_lrs, o[0], P.w_decay * w[0])),
+              const float w[4] = {__uint_as_float(wv[g].x), __uint_as_float(wv[g].y), __uint_as_float(wv[g].z),
+                                  __uint_as_float(wv[g].w)};
+              ptx::st_global_v4(wrow + gj0 + 4 * g, __float_as_uint(fmaf(-P.w_lrs, o[0], P.w_decay * w[0])),
                                 __float_as_uint(fmaf(-P.w_lrs, o[1], P.w_decay * w[1])),
                                 __float_as_uint(fmaf(-P.w_lrs, o[2], P.w_decay * w[2])),
                                 __float_as_uint(fmaf(-P.w_lrs, o[3], P.w_decay * w[3])));
             }
           }
+#pragma unroll
+          for (int g = 0; g < (kW ? 8 : 1); ++g) wv[g] = wn[g];
 #pragma unroll
           for (int g = 0; g < kAV; ++g) av[g] = an[g];
           continue;

@@ -1,0 +1,25 @@
+// Instantiations of the tensor-core kernel for the last update product of a
+// Muon step (a X + B X, or a Y + Y B for tall inputs, bf16 operands), whose
+// epilogue writes W = (1 - lr wd) W - lr scale bf16(X') into the fp32 master
+// weights instead of storing X'.  Always 4 epilogue warps: the prefetched
+// master-weight rows need the registers that 8 warps would not leave.
+#include "gemm_launch.cuh"
+
+namespace mns {
+
+template <bool B_MN>
+cudaError_t launch_full_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream) {
+  if (mode == kSingle) return cudaErrorInvalidValue;
+  return mode == kPairMma ? launch_tc_gemm<false, B_MN, false, 4, false, 2, true, true>(p, grid, stream)
+                          : launch_tc_gemm<false, B_MN, false, 4, false, 2, false, true>(p, grid, stream);
+}
+
+cudaError_t launch_full_kmn_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream) {
+  return launch_full_w<true>(p, mode, grid, stream);
+}
+
+cudaError_t launch_full_kk_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream) {
+  return launch_full_w<false>(p, mode, grid, stream);
+}
+
+}  // namespace mns

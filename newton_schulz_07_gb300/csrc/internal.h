@@ -54,6 +54,11 @@ cudaError_t launch_sym_mnmn(const GemmParams& p, PairMode mode, int grid, cudaSt
 cudaError_t launch_full_kmn(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
 cudaError_t launch_full_kk(const GemmParams& p, PairMode mode, int max_k, int grid, cudaStream_t stream);
 
+// The last update of a Muon step (GroupArgs::w_out): bf16 update products
+// whose epilogue writes the fp32 master weights; always 4 epilogue warps.
+cudaError_t launch_full_kmn_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+
 // The same for fp32 operands and outputs (tf32 tensor cores).
 cudaError_t launch_sym_kk_f32(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
 cudaError_t launch_sym_mnmn_f32(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);

@@ -24,6 +24,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -398,8 +399,14 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   for (int i = 0; i < ng; ++i)
     if (io[i].p.m > max_k) max_k = static_cast<int>(io[i].p.m);
   const mns::PairMode mode = mns::pair_mode(f32, max_k);
+  // The Muon step's last update (master-weight output) runs its own kernels,
+  // always with 4 epilogue warps.
+  bool wout = false;
+  for (int i = 0; i < ng; ++i) wout = wout || io[i].W != nullptr;
+  for (int i = 0; wout && i < ng; ++i)
+    if (io[i].W == nullptr) return MUON_NS_ERR_INVALID_ARG;  // all groups of a launch or none
   // The 4-warp bf16 update writes 32 x 64 output boxes.
-  const bool wide_out = !f32 && mns::update_epi_warps(mode, max_k) == 4;
+  const bool wide_out = !f32 && (wout || mns::update_epi_warps(mode, max_k) == 4);
   if (!f32 && P->out_t) return MUON_NS_ERR_INVALID_ARG;  // transposed outputs are fp32 only
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
@@ -451,6 +458,8 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   if (f32)
     return to_status(T ? mns::launch_full_kk_f32(*P, mode, max_k, grid, st)
                        : mns::launch_full_kmn_f32(*P, mode, max_k, grid, st));
+  if (wout)
+    return to_status(T ? mns::launch_full_kk_w(*P, mode, grid, st) : mns::launch_full_kmn_w(*P, mode, grid, st));
   return to_status(T ? mns::launch_full_kk(*P, mode, max_k, grid, st)
                      : mns::launch_full_kmn(*P, mode, max_k, grid, st));
 }
@@ -1001,18 +1010,52 @@ inline int host_chunk(long long batch, long long rows, long long cols, int chunk
   return static_cast<int>(c < 1 ? 1 : c);
 }
 
-// Size of chunk i of a host-path call with largest chunk c: the first and
-// (when the stack spans more than one chunk) the last take ceil(c / 2)
-// matrices, the ones in between c, the one before the last the remainder.
-// Returns 0 past the end.
-inline int host_chunk_size(int batch, int c, int i) {
-  if (batch <= c) return i == 0 ? batch : 0;
-  const int h = (c + 1) / 2;
-  const int mid = batch - 2 * h;  // matrices between the half-size ends (>= 0 since c < batch)
-  const int nmid = (mid + c - 1) / c;
-  if (i == 0) return h;
-  if (i <= nmid) return (i < nmid) ? c : mid - (nmid - 1) * c;
-  return i == nmid + 1 ? h : 0;
+// Chunk plan of a host-path call with largest chunk c (sizes in matrices,
+// in order; every size <= c, the sum is the batch).
+//   ramp == false (an explicit chunk argument): the first and, when the stack
+//     spans more than one chunk, the last take ceil(c / 2), the ones between c,
+//     the one before the last the remainder;
+//   ramp == true (the default chunk): the ends ramp h, 2h, 4h, ... (each < c,
+//     h = ceil(c / 8)) up at the start and down at the end, and the middle is
+//     split into ceil(middle / c) near-equal chunks.  The first upload and the
+//     last download, which nothing overlaps, then move about c / 8 matrices
+//     instead of c / 2.  Ramp steps are dropped, largest first, while the two
+//     ramps would leave less than one full chunk in the middle; with no step
+//     left the plan is the plain one.
+void host_plan(int batch, int c, bool ramp, std::vector<int>* plan) {
+  plan->clear();
+  if (batch <= 0) return;
+  if (batch <= c) {
+    plan->push_back(batch);
+    return;
+  }
+  std::vector<int> up;
+  if (ramp) {
+    const int h = (c + 7) / 8;
+    for (long long v = h; v < c; v *= 2) up.push_back(static_cast<int>(v));
+    long long sum = 0;
+    for (int v : up) sum += v;
+    while (!up.empty() && 2 * sum > static_cast<long long>(batch) - c) {
+      sum -= up.back();
+      up.pop_back();
+    }
+  }
+  if (up.empty()) {
+    const int h = (c + 1) / 2;
+    const int mid = batch - 2 * h;  // >= 0 since c < batch
+    const int nmid = (mid + c - 1) / c;
+    plan->push_back(h);
+    for (int i = 1; i <= nmid; ++i) plan->push_back(i < nmid ? c : mid - (nmid - 1) * c);
+    plan->push_back(h);
+    return;
+  }
+  long long sum = 0;
+  for (int v : up) sum += v;
+  const int mid = batch - 2 * static_cast<int>(sum);
+  const int n = (mid + c - 1) / c;
+  *plan = up;
+  for (int i = 0; i < n; ++i) plan->push_back(mid / n + (i < mid % n ? 1 : 0));
+  for (auto it = up.rbegin(); it != up.rend(); ++it) plan->push_back(*it);
 }
 
 // Host-path workspace: the call's error word, then two slots of (input
@@ -1059,6 +1102,18 @@ int muon_ns_host_chunk(int batch, int rows, int cols, int chunk) {
   return host_chunk(batch, rows, cols, chunk);
 }
 
+int muon_ns_host_plan(int batch, int rows, int cols, int chunk, int* sizes, int max_chunks) {
+  Problem p;
+  bool empty;
+  if (check_shape(batch, rows, cols, &p, &empty) != MUON_NS_OK || max_chunks < 0) return -1;
+  if (empty) return 0;
+  std::vector<int> plan;
+  host_plan(batch, host_chunk(batch, rows, cols, chunk), chunk <= 0, &plan);
+  if (sizes != nullptr)
+    for (int i = 0; i < static_cast<int>(plan.size()) && i < max_chunks; ++i) sizes[i] = plan[i];
+  return static_cast<int>(plan.size());
+}
+
 int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int rows, int cols,
                  int steps, const float* coeffs, float eps, int chunk, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream) {
@@ -1096,12 +1151,12 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
       cudaStreamWaitEvent(hp.up, hp.start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp.down, hp.start, 0) != cudaSuccess)
     return fail();
+  std::vector<int> plan;
+  host_plan(batch, cb, chunk <= 0, &plan);
   long long b0 = 0;
-  int nchunks = 0;
-  for (int i = 0;; ++i) {
-    const int nb = host_chunk_size(batch, cb, i);
-    if (nb == 0) break;
-    nchunks = i + 1;
+  const int nchunks = static_cast<int>(plan.size());
+  for (int i = 0; i < nchunks; ++i) {
+    const int nb = plan[i];
     const int sl = i % kHostSlots;
     const size_t bytes = 2 * mat * nb;
     uint8_t* slot = base + 1024 + sl * H.slot;

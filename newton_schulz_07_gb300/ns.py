@@ -190,6 +190,17 @@ def host_chunk(batch: int, rows: int, cols: int, chunk: int = 0) -> int:
     return _lib.lib().muon_ns_host_chunk(int(batch), int(rows), int(cols), int(chunk))
 
 
+def host_plan(batch: int, rows: int, cols: int, chunk: int = 0) -> list:
+    """Chunk sizes, in order, that muon_ns_host uses for this stack and `chunk`."""
+    L = _lib.lib()
+    n = L.muon_ns_host_plan(int(batch), int(rows), int(cols), int(chunk), None, 0)
+    if n < 0:
+        raise ValueError("invalid stack shape")
+    arr = (ctypes.c_int * max(n, 1))()
+    L.muon_ns_host_plan(int(batch), int(rows), int(cols), int(chunk), ctypes.cast(arr, ctypes.c_void_p), n)
+    return list(arr[:n])
+
+
 def set_wait_budget(cycles: int) -> None:
     """Budget of every bounded wait in the kernels, in SM clock cycles (0: the
     default, about 2 s).  A wait that runs out sets the device error word."""

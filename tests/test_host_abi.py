@@ -367,6 +367,30 @@ def test_host_path_workspace_arithmetic():
     assert ws(0, 256, 512) == 0
 
 
+def test_host_plan_covers_the_stack():
+    # Explicit chunk: half-size ends around full chunks, the remainder before the last.
+    assert ns.host_plan(10, 136, 264, 3) == [2, 3, 3, 2]
+    assert ns.host_plan(10, 136, 264, 4) == [2, 4, 2, 2]
+    assert ns.host_plan(10, 136, 264, 9) == [5, 5]
+    assert ns.host_plan(10, 136, 264, 100) == [10]
+    # Default: ends ramping from about an eighth of the largest chunk.
+    assert ns.host_plan(128, 1536, 2048) == [2, 4, 8, 15, 15, 14, 14, 14, 14, 14, 8, 4, 2]
+    assert ns.host_plan(32, 7168, 2048) == [1, 2, 4, 4, 4, 4, 4, 3, 3, 2, 1]
+    assert ns.host_plan(128, 2048, 768) == [4, 8, 16, 24, 24, 24, 16, 8, 4]
+    assert ns.host_plan(16, 1536, 2048) == [1, 2, 5, 5, 2, 1]
+    assert ns.host_plan(16, 256, 512) == [16]  # under 32 MiB: one chunk
+    for shape in [(128, 1536, 2048), (32, 7168, 2048), (128, 2048, 768), (16, 1536, 2048), (17, 1536, 2048),
+                  (3, 4096, 4096), (1, 8192, 8192), (1000, 1024, 1024), (10, 136, 264)]:
+        for chunk in (0, 1, 2, 3, 7, 16):
+            plan = ns.host_plan(*shape, chunk)
+            c = ns.host_chunk(*shape, chunk)
+            assert sum(plan) == shape[0] and all(1 <= v <= c for v in plan), (shape, chunk, plan)
+            assert plan == plan[::-1] or chunk > 0 or len(plan) == 1 or plan[0] <= (c + 7) // 8
+    assert ns.host_plan(0, 256, 512) == []
+    with pytest.raises(ValueError):
+        ns.host_plan(2, 12, 8)
+
+
 def test_host_path_argument_errors():
     assert _call_host(G=0) == _lib.ERR_INVALID_ARG
     assert _call_host(out=0) == _lib.ERR_INVALID_ARG
