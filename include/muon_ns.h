@@ -238,17 +238,13 @@ int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, cons
 /* Device workspace bytes for muon_ns_host(): the call's error word (256
  * bytes, then padding to 1 KB) and two slots of (input chunk, output chunk,
  * muon_ns_ws() workspace of one chunk of `chunk` matrices).  `chunk` is the
- * largest chunk; chunk > batch is clamped to batch.  With an explicit chunk,
- * a stack larger than it is split into a first and a last chunk of
+ * largest chunk: when the stack is larger, the first and the last chunk take
  * ceil(chunk / 2) matrices (shorter upload before the first compute and
- * download after the last) and chunks of `chunk` between them, the one
- * before the last taking the remainder.  chunk <= 0 selects the default: the
- * whole stack if it holds less than 32 MiB, else a largest chunk c of
- * ceil(96 MiB / (2 * rows * cols)) matrices but at most ceil(batch / 2), with
- * ends that ramp h, 2h, 4h, ... (each < c, h = ceil(c / 8)) up at the start
- * and down at the end around near-equal middle chunks of at most c, so that
- * the copies nothing overlaps move about c / 8 matrices each
- * (muon_ns_host_plan gives the sizes).  Returns MUON_NS_OK or
+ * download after the last) and the ones between `chunk`, the one before the
+ * last the remainder (muon_ns_host_plan gives the sizes).  chunk <= 0 selects
+ * the default: the whole stack if it holds less than 32 MiB, else
+ * ceil(96 MiB / (2 * rows * cols)) matrices but at most ceil(batch / 2).
+ * chunk > batch is clamped to batch.  Returns MUON_NS_OK or
  * MUON_NS_ERR_INVALID_ARG / MUON_NS_ERR_ALIGNMENT as muon_ns_workspace_size(). */
 int muon_ns_host_workspace_size(int batch, int rows, int cols, int chunk, size_t* bytes);
 

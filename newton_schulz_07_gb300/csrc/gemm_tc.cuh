@@ -795,25 +795,27 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       // A row tile past the last one (second CTA of a cluster, odd row-tile
       // count) was computed on zero-filled operands: nothing to store.
       const int n_chunks = (CL == 2 && I * kTileM >= G.M) ? 0 : kChunksPerWarp;
-      // Muon step (GroupArgs::w_out): this lane's row of the master weights,
-      // 32 fp32 columns per chunk, is loaded one chunk ahead; chunk 0 before
-      // the accumulator wait, which hides its latency.  W is written by no
-      // other kernel of the call, so it may be read early.
+      // Muon step (GroupArgs::w_out): the master weights of this warp's 32
+      // rows are read and written coalesced, lane l taking row 4 it + l / 8,
+      // columns 4 (l % 8) .. + 3 of a chunk in pass it = 0..7, and loaded
+      // one chunk ahead; chunk 0 before the accumulator wait, which hides its
+      // latency.  W is written by no other kernel of the call, so it may be
+      // read early.
       constexpr bool kW = WOUT;
       const bool wmode = kW && G.w_out != nullptr;
-      float* wrow = nullptr;
+      float* wbase = wmode ? G.w_out + static_cast<long long>(b) * G.bstride : nullptr;
+      const int wr0 = I * kTileM + q * 32;  // first row of this warp
       uint4 wv[kW ? 8 : 1];
       auto load_w = [&](int cc, uint4 (&dst)[kW ? 8 : 1]) {
-        const int gj0 = J * kTileN + (c_begin + cc) * 32;
+        const int col = J * kTileN + (c_begin + cc) * 32 + 4 * (lane & 7);
 #pragma unroll
-        for (int g = 0; g < (kW ? 8 : 1); ++g)
-          if (wrow != nullptr && gj0 + 4 * g + 4 <= G.N) dst[g] = ptx::ld_global_v4(wrow + gj0 + 4 * g);
+        for (int it = 0; it < (kW ? 8 : 1); ++it) {
+          const int row = wr0 + 4 * it + (lane >> 3);
+          if (row < G.M && col + 4 <= G.N)
+            dst[it] = ptx::ld_global_v4(wbase + static_cast<long long>(row) * G.ld + col);
+        }
       };
-      if (wmode) {
-        const long long wi = static_cast<long long>(I) * kTileM + r_in_tile;
-        if (wi < G.M && n_chunks > 0) wrow = G.w_out + static_cast<long long>(b) * G.bstride + wi * G.ld;
-        load_w(0, wv);
-      }
+      if (wmode && n_chunks > 0) load_w(0, wv);
       int ready = 0;
       if (lane == 0)
         ready = detail::wait_bounded<SM2>(sy.tfull(buf), tphase, abort_flag, P.err, P.budget) ? 1 : 0;
@@ -944,26 +946,38 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         }
         if (wmode) {
           // Muon step: the master weights take this chunk's values in place
-          // of the stored iterate, w = w_decay w - w_lrs bf16(f) (16-byte
-          // loads and stores of this lane's row; N is a multiple of 8, so a
-          // 4-column group is wholly in or out).
+          // of the stored iterate, w = w_decay w - w_lrs bf16(f).  The rounded
+          // values go through the warp's staging chunk (fp32, 128-byte rows,
+          // 128-byte swizzle: conflict-free both ways), so that W moves in
+          // whole 128-byte rows.
           uint4 wn[kW ? 8 : 1];
           if (cc + 1 < n_chunks) load_w(cc + 1, wn);
-          if (wrow != nullptr) {
 #pragma unroll
-            for (int g = 0; g < (kW ? 8 : 1); ++g) {
-              if (gj0 + 4 * g + 4 > G.N) break;
-              const uint32_t lo = detail::pack_bf16x2(f[4 * g], f[4 * g + 1]);
-              const uint32_t hi = detail::pack_bf16x2(f[4 * g + 2], f[4 * g + 3]);
-              const float o[4] = {detail::bf16_lo(lo), detail::bf16_hi(lo), detail::bf16_lo(hi), detail::bf16_hi(hi)};
-              const float w[4] = {__uint_as_float(wv[g].x), __uint_as_float(wv[g].y), __uint_as_float(wv[g].z),
-                                  __uint_as_float(wv[g].w)};
-              ptx::st_global_v4(wrow + gj0 + 4 * g, __float_as_uint(fmaf(-P.w_lrs, o[0], P.w_decay * w[0])),
-                                __float_as_uint(fmaf(-P.w_lrs, o[1], P.w_decay * w[1])),
-                                __float_as_uint(fmaf(-P.w_lrs, o[2], P.w_decay * w[2])),
-                                __float_as_uint(fmaf(-P.w_lrs, o[3], P.w_decay * w[3])));
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t lo = detail::pack_bf16x2(f[4 * g], f[4 * g + 1]);
+            const uint32_t hi = detail::pack_bf16x2(f[4 * g + 2], f[4 * g + 3]);
+            ptx::st_shared_v4(stg + stage_off32(lane, 4 * g), lo << 16, lo & 0xFFFF0000u, hi << 16,
+                              hi & 0xFFFF0000u);
+          }
+          __syncwarp();
+          const int col = gj0 + 4 * (lane & 7);
+#pragma unroll
+          for (int it = 0; it < (kW ? 8 : 1); ++it) {
+            const int rr = 4 * it + (lane >> 3);
+            const int row = wr0 + rr;
+            if (row < G.M && col + 4 <= G.N) {
+              uint32_t o4[4];
+              ptx::ld_shared_v4(stg + stage_off32(rr, 4 * (lane & 7)), o4);
+              const float w[4] = {__uint_as_float(wv[it].x), __uint_as_float(wv[it].y),
+                                  __uint_as_float(wv[it].z), __uint_as_float(wv[it].w)};
+              ptx::st_global_v4(wbase + static_cast<long long>(row) * G.ld + col,
+                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[0]), P.w_decay * w[0])),
+                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[1]), P.w_decay * w[1])),
+                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[2]), P.w_decay * w[2])),
+                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[3]), P.w_decay * w[3])));
             }
           }
+          __syncwarp();  // the staging chunk is rewritten by the next chunk
 #pragma unroll
           for (int g = 0; g < (kW ? 8 : 1); ++g) wv[g] = wn[g];
 #pragma unroll

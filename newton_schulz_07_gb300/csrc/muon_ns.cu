@@ -1011,51 +1011,25 @@ inline int host_chunk(long long batch, long long rows, long long cols, int chunk
 }
 
 // Chunk plan of a host-path call with largest chunk c (sizes in matrices,
-// in order; every size <= c, the sum is the batch).
-//   ramp == false (an explicit chunk argument): the first and, when the stack
-//     spans more than one chunk, the last take ceil(c / 2), the ones between c,
-//     the one before the last the remainder;
-//   ramp == true (the default chunk): the ends ramp h, 2h, 4h, ... (each < c,
-//     h = ceil(c / 8)) up at the start and down at the end, and the middle is
-//     split into ceil(middle / c) near-equal chunks.  The first upload and the
-//     last download, which nothing overlaps, then move about c / 8 matrices
-//     instead of c / 2.  Ramp steps are dropped, largest first, while the two
-//     ramps would leave less than one full chunk in the middle; with no step
-//     left the plan is the plain one.
-void host_plan(int batch, int c, bool ramp, std::vector<int>* plan) {
+// in order; every size <= c, the sum is the batch): when the stack spans more
+// than one chunk, the first and the last take ceil(c / 2) (shorter copies
+// before the first compute and after the last, which nothing overlaps), the
+// ones between c, the one before the last the remainder.  (Ends that ramp
+// c / 8, c / 4, c / 2 were measured slower on every stack: each extra chunk
+// pays a whole call's chain of launches on a GPU it does not fill.)
+void host_plan(int batch, int c, std::vector<int>* plan) {
   plan->clear();
   if (batch <= 0) return;
   if (batch <= c) {
     plan->push_back(batch);
     return;
   }
-  std::vector<int> up;
-  if (ramp) {
-    const int h = (c + 7) / 8;
-    for (long long v = h; v < c; v *= 2) up.push_back(static_cast<int>(v));
-    long long sum = 0;
-    for (int v : up) sum += v;
-    while (!up.empty() && 2 * sum > static_cast<long long>(batch) - c) {
-      sum -= up.back();
-      up.pop_back();
-    }
-  }
-  if (up.empty()) {
-    const int h = (c + 1) / 2;
-    const int mid = batch - 2 * h;  // >= 0 since c < batch
-    const int nmid = (mid + c - 1) / c;
-    plan->push_back(h);
-    for (int i = 1; i <= nmid; ++i) plan->push_back(i < nmid ? c : mid - (nmid - 1) * c);
-    plan->push_back(h);
-    return;
-  }
-  long long sum = 0;
-  for (int v : up) sum += v;
-  const int mid = batch - 2 * static_cast<int>(sum);
-  const int n = (mid + c - 1) / c;
-  *plan = up;
-  for (int i = 0; i < n; ++i) plan->push_back(mid / n + (i < mid % n ? 1 : 0));
-  for (auto it = up.rbegin(); it != up.rend(); ++it) plan->push_back(*it);
+  const int h = (c + 1) / 2;
+  const int mid = batch - 2 * h;  // >= 0 since c < batch
+  const int nmid = (mid + c - 1) / c;
+  plan->push_back(h);
+  for (int i = 1; i <= nmid; ++i) plan->push_back(i < nmid ? c : mid - (nmid - 1) * c);
+  plan->push_back(h);
 }
 
 // Host-path workspace: the call's error word, then two slots of (input
@@ -1108,7 +1082,7 @@ int muon_ns_host_plan(int batch, int rows, int cols, int chunk, int* sizes, int 
   if (check_shape(batch, rows, cols, &p, &empty) != MUON_NS_OK || max_chunks < 0) return -1;
   if (empty) return 0;
   std::vector<int> plan;
-  host_plan(batch, host_chunk(batch, rows, cols, chunk), chunk <= 0, &plan);
+  host_plan(batch, host_chunk(batch, rows, cols, chunk), &plan);
   if (sizes != nullptr)
     for (int i = 0; i < static_cast<int>(plan.size()) && i < max_chunks; ++i) sizes[i] = plan[i];
   return static_cast<int>(plan.size());
@@ -1152,7 +1126,7 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
       cudaStreamWaitEvent(hp.down, hp.start, 0) != cudaSuccess)
     return fail();
   std::vector<int> plan;
-  host_plan(batch, cb, chunk <= 0, &plan);
+  host_plan(batch, cb, &plan);
   long long b0 = 0;
   const int nchunks = static_cast<int>(plan.size());
   for (int i = 0; i < nchunks; ++i) {

@@ -373,11 +373,11 @@ def test_host_plan_covers_the_stack():
     assert ns.host_plan(10, 136, 264, 4) == [2, 4, 2, 2]
     assert ns.host_plan(10, 136, 264, 9) == [5, 5]
     assert ns.host_plan(10, 136, 264, 100) == [10]
-    # Default: ends ramping from about an eighth of the largest chunk.
-    assert ns.host_plan(128, 1536, 2048) == [2, 4, 8, 15, 15, 14, 14, 14, 14, 14, 8, 4, 2]
-    assert ns.host_plan(32, 7168, 2048) == [1, 2, 4, 4, 4, 4, 4, 3, 3, 2, 1]
-    assert ns.host_plan(128, 2048, 768) == [4, 8, 16, 24, 24, 24, 16, 8, 4]
-    assert ns.host_plan(16, 1536, 2048) == [1, 2, 5, 5, 2, 1]
+    # Default largest chunk, same shape of plan.
+    assert ns.host_plan(128, 1536, 2048) == [8] + [16] * 7 + [8]
+    assert ns.host_plan(32, 7168, 2048) == [2] + [4] * 7 + [2]
+    assert ns.host_plan(128, 2048, 768) == [16, 32, 32, 32, 16]
+    assert ns.host_plan(16, 1536, 2048) == [4, 8, 4]
     assert ns.host_plan(16, 256, 512) == [16]  # under 32 MiB: one chunk
     for shape in [(128, 1536, 2048), (32, 7168, 2048), (128, 2048, 768), (16, 1536, 2048), (17, 1536, 2048),
                   (3, 4096, 4096), (1, 8192, 8192), (1000, 1024, 1024), (10, 136, 264)]:
@@ -385,7 +385,7 @@ def test_host_plan_covers_the_stack():
             plan = ns.host_plan(*shape, chunk)
             c = ns.host_chunk(*shape, chunk)
             assert sum(plan) == shape[0] and all(1 <= v <= c for v in plan), (shape, chunk, plan)
-            assert plan == plan[::-1] or chunk > 0 or len(plan) == 1 or plan[0] <= (c + 7) // 8
+            assert len(plan) == 1 or plan[0] == plan[-1] == (c + 1) // 2
     assert ns.host_plan(0, 256, 512) == []
     with pytest.raises(ValueError):
         ns.host_plan(2, 12, 8)
