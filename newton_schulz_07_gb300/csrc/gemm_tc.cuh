@@ -92,6 +92,13 @@ constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
 #ifndef MNS_DIAG_ONCE
 #define MNS_DIAG_ONCE 1
 #endif
+// Output chunks leave shared memory through bulk tensor stores (the TMA unit,
+// shared with the producer's operand loads) or, with MNS_LSU_STORES=1, through
+// coalesced 16-byte stores of the epilogue warp's lanes (whole 64- or 128-byte
+// row pieces, clipped to the output's rows and columns).
+#ifndef MNS_LSU_STORES
+#define MNS_LSU_STORES 0
+#endif
 
 
 // Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
@@ -231,6 +238,10 @@ struct GroupArgs {
   //   w_out[b][i][j] = w_decay * w_out[b][i][j] - w_lrs * o,
   // with w_out laid out like the output ([batch][M][N], row stride ld).
   float* w_out;
+  // The outputs' base addresses (the same tensors as tmOut / tmOutT), for
+  // the epilogue's coalesced stores under MNS_LSU_STORES.
+  void* out;
+  void* out_t;
 };
 
 // Counter increment per finished unit of the tile space, whatever the
@@ -1008,9 +1019,54 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
                               w[4 * g + 3]);
         };
         // Stage the chunk in shared memory and write it with bulk tensor
-        // stores (rows beyond M or columns beyond N are clipped by the TMA).
+        // stores (rows beyond M or columns beyond N are clipped by the TMA), or
+        // read it back coalesced and store it from all lanes (MNS_LSU_STORES).
         const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
-        if (lane == 0) {
+        constexpr bool kLSU = MNS_LSU_STORES;
+        // Box of 32 rows staged at `src` to (row y, column x) of output
+        // `which` (0: [M][N], 1: the transposed [N][M]).
+        auto put = [&](uint32_t src, int x, int y, int which) {
+          if (!kLSU) {
+            if (lane == 0) ptx::tma_store_3d(which ? tmOutT : tmOut, src, x, y, b);
+            return;
+          }
+          constexpr int kRowBytes = (kWide || F32) ? 128 : 64;
+          constexpr int kGpr = kRowBytes / 16;   // 16-byte granules per row
+          constexpr int kRowsPerIt = 32 / kGpr;  // rows per warp-wide pass
+          constexpr int kEpg = 16 / EC::kBytes;  // elements per granule
+          const int rmax = which ? G.N : G.M;
+          const int cmax = which ? G.M : G.N;   // also the row stride
+          uint8_t* mat = static_cast<uint8_t*>(which ? G.out_t : G.out) +
+                         static_cast<long long>(b) * G.bstride * EC::kBytes;
+          const int g = lane % kGpr;
+#pragma unroll
+          for (int it = 0; it < kGpr; ++it) {
+            const int rr = it * kRowsPerIt + lane / kGpr;
+            const int row = y + rr, col = x + g * kEpg;
+            if (row < rmax && col + kEpg <= cmax) {
+              const uint32_t off = kWide ? stage_off_wide(rr, g) : (F32 ? stage_off32(rr, 4 * g) : stage_off(rr, 8 * g));
+              uint32_t v[4];
+              ptx::ld_shared_v4(src + off, v);
+              ptx::st_global_v4(mat + (static_cast<long long>(row) * cmax + col) * EC::kBytes, v[0], v[1], v[2], v[3]);
+            }
+          }
+        };
+        // Before a box is stored: its staging writes visible to the stores.
+        auto put_begin = [&]() {
+          if (!kLSU) ptx::fence_proxy_async_smem();
+          __syncwarp();
+        };
+        // After: one bulk group per stored chunk (TMA), or the staging free
+        // again once every lane has read it back (coalesced stores).
+        auto put_end = [&]() {
+          if (kLSU) {
+            __syncwarp();
+          } else if (lane == 0) {
+            ptx::bulk_commit();
+            ++groups;
+          }
+        };
+        if (lane == 0 && !kLSU) {
           if (kWide) {
             if (!(cc & 1)) ptx::bulk_wait_read<0>();
           } else if (kBufs == 2 && !SYM && !P.out_t) {
@@ -1032,13 +1088,11 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
                               w[4 * g + 2], w[4 * g + 3]);
           const bool more = cc + 1 < n_chunks && gj0 + 32 < G.N;
           if (h == 1 || !more) {
-            ptx::fence_proxy_async_smem();
+            put_begin();
+            put(stg, gj0 - h * 32, R0, 0);
+            put_end();
+          } else if (kLSU) {
             __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_3d(tmOut, stg, gj0 - h * 32, R0, b);
-              ptx::bulk_commit();
-            ++groups;
-            }
           }
         } else if (!SYM && P.out_t) {
           // The chunk at (R0, gj0) and its transpose at (gj0, R0) of the
@@ -1048,34 +1102,22 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           st_row(d);
 #pragma unroll
           for (int j = 0; j < 32; ++j) st_elem(tr + soff(j, lane), j);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
-            ptx::tma_store_3d(tmOutT, tr, R0, gj0, b);
-            ptx::bulk_commit();
-            ++groups;
-          }
+          put_begin();
+          put(d, gj0, R0, 0);
+          put(tr, R0, gj0, 1);
+          put_end();
         } else if (!SYM) {
           const uint32_t d = stg + static_cast<uint32_t>((kBufs == 2 ? (cc & 1) : 0) * kCB);
           st_row(d);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
-            ptx::bulk_commit();
-            ++groups;
-          }
+          put_begin();
+          put(d, gj0, R0, 0);
+          put_end();
         } else if (gj0 < R0 && P.half_out && (gj0 >> 8) != (R0 >> 8)) {
           // Half storage, outside the diagonal 256-block: the chunk alone.
           st_row(stg);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(tmOut, stg, gj0, R0, b);
-            ptx::bulk_commit();
-            ++groups;
-          }
+          put_begin();
+          put(stg, gj0, R0, 0);
+          put_end();
         } else if (gj0 < R0) {
           // Below the diagonal: the chunk at (R0, gj0) and its transpose at (gj0, R0).
           const uint32_t d = stg;
@@ -1083,14 +1125,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           st_row(d);
 #pragma unroll
           for (int j = 0; j < 32; ++j) st_elem(tr + soff(j, lane), j);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
-            ptx::tma_store_3d(tmOut, tr, R0, gj0, b);
-            ptx::bulk_commit();
-            ++groups;
-          }
+          put_begin();
+          put(d, gj0, R0, 0);
+          put(tr, R0, gj0, 0);
+          put_end();
         } else {
           // Diagonal 32 x 32 block (gj0 == R0): entry (r, j) takes the value
           // computed at (max(r, j), min(r, j)), so the block is bit-symmetric.
@@ -1100,13 +1138,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             if (j <= lane) st_elem(d + soff(lane, j), j);
             if (j < lane) st_elem(d + soff(j, lane), j);
           }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(tmOut, d, gj0, R0, b);
-            ptx::bulk_commit();
-            ++groups;
-          }
+          put_begin();
+          put(d, gj0, R0, 0);
+          put_end();
         }
 #pragma unroll
         for (int g = 0; g < kAV; ++g) av[g] = an[g];
