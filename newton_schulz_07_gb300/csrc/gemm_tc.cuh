@@ -92,13 +92,6 @@ constexpr int kTmemCols = 2 * kTileN;          // two fp32 accumulators
 #ifndef MNS_DIAG_ONCE
 #define MNS_DIAG_ONCE 1
 #endif
-// Output chunks leave shared memory through bulk tensor stores (the TMA unit,
-// shared with the producer's operand loads) or, with MNS_LSU_STORES=1, through
-// coalesced 16-byte stores of the epilogue warp's lanes (whole 64- or 128-byte
-// row pieces, clipped to the output's rows and columns).
-#ifndef MNS_LSU_STORES
-#define MNS_LSU_STORES 0
-#endif
 
 
 // Output staging: each epilogue warp stages 32 x 32 output chunks (bf16: 2 KB,
@@ -238,10 +231,6 @@ struct GroupArgs {
   //   w_out[b][i][j] = w_decay * w_out[b][i][j] - w_lrs * o,
   // with w_out laid out like the output ([batch][M][N], row stride ld).
   float* w_out;
-  // The outputs' base addresses (the same tensors as tmOut / tmOutT), for
-  // the epilogue's coalesced stores under MNS_LSU_STORES.
-  void* out;
-  void* out_t;
 };
 
 // Counter increment per finished unit of the tile space, whatever the
@@ -1019,54 +1008,26 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
                               w[4 * g + 3]);
         };
         // Stage the chunk in shared memory and write it with bulk tensor
-        // stores (rows beyond M or columns beyond N are clipped by the TMA), or
-        // read it back coalesced and store it from all lanes (MNS_LSU_STORES).
+        // stores (rows beyond M or columns beyond N are clipped by the TMA).
         const int R0 = I * kTileM + q * 32;  // first row of this warp (multiple of 32)
-        constexpr bool kLSU = MNS_LSU_STORES;
         // Box of 32 rows staged at `src` to (row y, column x) of output
         // `which` (0: [M][N], 1: the transposed [N][M]).
         auto put = [&](uint32_t src, int x, int y, int which) {
-          if (!kLSU) {
-            if (lane == 0) ptx::tma_store_3d(which ? tmOutT : tmOut, src, x, y, b);
-            return;
-          }
-          constexpr int kRowBytes = (kWide || F32) ? 128 : 64;
-          constexpr int kGpr = kRowBytes / 16;   // 16-byte granules per row
-          constexpr int kRowsPerIt = 32 / kGpr;  // rows per warp-wide pass
-          constexpr int kEpg = 16 / EC::kBytes;  // elements per granule
-          const int rmax = which ? G.N : G.M;
-          const int cmax = which ? G.M : G.N;   // also the row stride
-          uint8_t* mat = static_cast<uint8_t*>(which ? G.out_t : G.out) +
-                         static_cast<long long>(b) * G.bstride * EC::kBytes;
-          const int g = lane % kGpr;
-#pragma unroll
-          for (int it = 0; it < kGpr; ++it) {
-            const int rr = it * kRowsPerIt + lane / kGpr;
-            const int row = y + rr, col = x + g * kEpg;
-            if (row < rmax && col + kEpg <= cmax) {
-              const uint32_t off = kWide ? stage_off_wide(rr, g) : (F32 ? stage_off32(rr, 4 * g) : stage_off(rr, 8 * g));
-              uint32_t v[4];
-              ptx::ld_shared_v4(src + off, v);
-              ptx::st_global_v4(mat + (static_cast<long long>(row) * cmax + col) * EC::kBytes, v[0], v[1], v[2], v[3]);
-            }
-          }
+          if (lane == 0) ptx::tma_store_3d(which ? tmOutT : tmOut, src, x, y, b);
         };
-        // Before a box is stored: its staging writes visible to the stores.
+        // Before a box is stored: its staging writes visible to the async proxy.
         auto put_begin = [&]() {
-          if (!kLSU) ptx::fence_proxy_async_smem();
+          ptx::fence_proxy_async_smem();
           __syncwarp();
         };
-        // After: one bulk group per stored chunk (TMA), or the staging free
-        // again once every lane has read it back (coalesced stores).
+        // After: one bulk group per stored chunk.
         auto put_end = [&]() {
-          if (kLSU) {
-            __syncwarp();
-          } else if (lane == 0) {
+          if (lane == 0) {
             ptx::bulk_commit();
             ++groups;
           }
         };
-        if (lane == 0 && !kLSU) {
+        if (lane == 0) {
           if (kWide) {
             if (!(cc & 1)) ptx::bulk_wait_read<0>();
           } else if (kBufs == 2 && !SYM && !P.out_t) {
@@ -1091,8 +1052,6 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
             put_begin();
             put(stg, gj0 - h * 32, R0, 0);
             put_end();
-          } else if (kLSU) {
-            __syncwarp();
           }
         } else if (!SYM && P.out_t) {
           // The chunk at (R0, gj0) and its transpose at (gj0, R0) of the

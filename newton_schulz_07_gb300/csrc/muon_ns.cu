@@ -318,7 +318,6 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
     const Problem& p = io[i].p;
     set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32, mode);
     P->grp[i].norms = io[i].norms;
-    P->grp[i].out = io[i].A;
     // Signals the Gram counter; waits for the previous step's update.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep;
     if (all_have_dep(io, ng) && io[i].step > 0) {
@@ -361,7 +360,6 @@ int run_poly(const StepIO* io, int ng, float b, float c, int* err, int sms, cuda
     set_group(P, i, 1, batch, m, m, m, &total, f32, mode);
     P->grp[i].addend = io[i].A;
     P->grp[i].diag_out = io[i].D;
-    P->grp[i].out = io[i].B;
     // Signals the poly counter; waits for this step's Gram.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + batch;
     if (all_have_dep(io, ng)) {
@@ -430,8 +428,6 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     P->grp[i].addend = io[i].X;
     P->grp[i].diag_in = io[i].D;
     P->grp[i].norms = io[i].norms;
-    P->grp[i].out = io[i].Xn;
-    P->grp[i].out_t = io[i].Xt;
     if (io[i].W != nullptr) {
       if (f32) return MUON_NS_ERR_INVALID_ARG;  // the Muon step runs the bf16 NS
       P->grp[i].w_out = io[i].W;
