@@ -154,6 +154,36 @@ def test_argument_errors():
     assert ns.read_error(ws) == 0
 
 
+def test_step_captured_in_a_graph_equals_eager_steps():
+    # muon_step_ws allocates nothing and does not synchronise: two replays of a
+    # captured step give the bits of two eager steps on the same state.
+    shape = (3, 256, 512)
+    W, M, G = f32_stack(shape, 16), f32_stack(shape, 17, 0.05), f32_stack(shape, 18, 0.05)
+    kw = dict(lr=0.02, momentum=0.9, weight_decay=0.01)
+    Wd, Md, Gd = (torch.from_numpy(x).cuda() for x in (W, M, G))
+    ws = torch.empty(ns.step_workspace_size(*shape), dtype=torch.uint8, device="cuda")
+    We, Me = Wd.clone(), Md.clone()
+    for _ in range(2):
+        ns.muon_step(We, Me, Gd, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    Wx, Mx = Wd.clone(), Md.clone()
+    with torch.cuda.stream(side):  # first launches (per-device set-up) outside the capture
+        ns.muon_step(Wx, Mx, Gd, workspace=ws, **kw)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ns.muon_step(Wd, Md, Gd, workspace=ws, **kw)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert ns.read_error(ws) == 0
+    np.testing.assert_array_equal(Md.cpu().numpy(), Me.cpu().numpy())
+    np.testing.assert_array_equal(Wd.cpu().numpy().view(np.uint32), We.cpu().numpy().view(np.uint32))
+
+
 @pytest.mark.slow
 def test_full_size_expert_stack_sampled():
     w = ns_inputs.WORKLOADS["experts_128x1536x2048"]
