@@ -416,3 +416,55 @@ def test_wait_budget_and_stall_injection_settings():
     assert L.muon_ns_set_wait_budget(0) == _lib.OK
     assert L.muon_ns_inject_stall(1) == _lib.OK
     assert L.muon_ns_inject_stall(0) == _lib.OK
+
+
+# ----------------------------------------------------------------- Muon step --
+
+def _call_step(**kw):
+    # Fake, distinct, 16-byte aligned addresses: every check below returns
+    # before the library touches a device or dereferences a pointer.
+    L = _lib.lib()
+    args = dict(W=1 << 20, M=2 << 20, G=3 << 20, batch=2, rows=64, cols=128, steps=5, eps=1e-7,
+                ws=1 << 24, wsb=1 << 30, hp=_lib.MuonStepHparams(0.02, 0.95, 0.0, 1.0, 1))
+    args.update(kw)
+    hp = args["hp"]
+    return L.muon_step_ws(ctypes.c_void_p(args["W"]), ctypes.c_void_p(args["M"]), ctypes.c_void_p(args["G"]),
+                          args["batch"], args["rows"], args["cols"], None if hp is None else ctypes.byref(hp),
+                          args["steps"], None, ctypes.c_float(args["eps"]), ctypes.c_void_p(args["ws"]), args["wsb"],
+                          None)
+
+
+def test_muon_step_argument_errors():
+    nan = float("nan")
+    assert _call_step(W=0) == _lib.ERR_INVALID_ARG
+    assert _call_step(M=0) == _lib.ERR_INVALID_ARG
+    assert _call_step(G=0) == _lib.ERR_INVALID_ARG
+    assert _call_step(hp=None) == _lib.ERR_INVALID_ARG
+    for bad in (_lib.MuonStepHparams(nan, 0.95, 0.0, 1.0, 1), _lib.MuonStepHparams(0.02, float("inf"), 0.0, 1.0, 1),
+                _lib.MuonStepHparams(0.02, 0.95, nan, 1.0, 1), _lib.MuonStepHparams(0.02, 0.95, 0.0, nan, 1)):
+        assert _call_step(hp=bad) == _lib.ERR_INVALID_ARG
+    nbytes = 4 * 2 * 64 * 128
+    assert _call_step(M=(1 << 20) + nbytes - 16) == _lib.ERR_INVALID_ARG  # W and M overlap
+    assert _call_step(G=(2 << 20) + 16) == _lib.ERR_INVALID_ARG  # M and G overlap
+    assert _call_step(W=(1 << 20) + 4) == _lib.ERR_ALIGNMENT
+    assert _call_step(rows=60) == _lib.ERR_ALIGNMENT
+    assert _call_step(steps=-1) == _lib.ERR_INVALID_ARG
+    assert _call_step(eps=-1.0) == _lib.ERR_INVALID_ARG
+    assert _call_step(wsb=1024) == _lib.ERR_WORKSPACE
+    assert _call_step(ws=0) == _lib.ERR_WORKSPACE
+    assert _call_step(ws=(1 << 24) + 16) == _lib.ERR_ALIGNMENT
+    assert _call_step(batch=0) == _lib.OK  # empty stack: nothing to do
+
+
+def test_muon_step_workspace_and_launch_count():
+    ws = ns.step_workspace_size(2, 64, 128)
+    # The NS workspace of the stack, then U (bf16) rounded up to 1 KiB.
+    assert ws == -(-ns.workspace_size(2, 64, 128) // 1024) * 1024 + -(-(2 * 2 * 64 * 128) // 1024) * 1024
+    assert ns.step_workspace_size(0, 64, 128) == 0
+    assert ns.step_launches(5) == 16 and ns.step_launches(0) == 3 and ns.step_launches(-1) == -1
+    assert ns.default_scale(2048, 768) == (2048 / 768) ** 0.5 and ns.default_scale(768, 2048) == 1.0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_muon_step_without_device_is_unsupported():
+    assert _call_step() == _lib.ERR_UNSUPPORTED_DEVICE
