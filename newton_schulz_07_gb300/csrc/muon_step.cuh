@@ -71,38 +71,42 @@ __global__ void __launch_bounds__(kNormThreads)
   const long long mat = static_cast<long long>(b) * vec_per_matrix;
   const long long base = static_cast<long long>(chunk) * kNormChunkVec;
 
-  // All loads of the thread first (16 fp32 vectors in flight), then the
-  // arithmetic and the stores.
-  float4 g[2 * kNormVecPerThread], m[2 * kNormVecPerThread];
+  // The thread's vectors in two halves: the loads of a half (8 fp32 vectors
+  // in flight), then its arithmetic and stores.  Halves keep the registers
+  // low enough for several CTAs per SM; the norm still adds the vectors'
+  // sums of squares in the order ns_norm_partial does.
+  constexpr int kHalf = kNormVecPerThread / 2;
+  float acc = 0.0f;
 #pragma unroll
-  for (int it = 0; it < kNormVecPerThread; ++it) {
-    const long long i = base + it * kNormThreads + threadIdx.x;
-    if (i < vec_per_matrix) {
-      const long long v = 2 * (mat + i);
-      g[2 * it] = __ldcs(G + v);
-      g[2 * it + 1] = __ldcs(G + v + 1);
-      m[2 * it] = M[v];
-      m[2 * it + 1] = M[v + 1];
+  for (int h = 0; h < 2; ++h) {
+    float4 g[2 * kHalf], m[2 * kHalf];
+#pragma unroll
+    for (int q = 0; q < kHalf; ++q) {
+      const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
+      if (i < vec_per_matrix) {
+        const long long v = 2 * (mat + i);
+        g[2 * q] = __ldcs(G + v);
+        g[2 * q + 1] = __ldcs(G + v + 1);
+        m[2 * q] = M[v];
+        m[2 * q + 1] = M[v + 1];
+      }
     }
-  }
-  uint4 u[kNormVecPerThread];
 #pragma unroll
-  for (int it = 0; it < kNormVecPerThread; ++it) {
-    const long long i = base + it * kNormThreads + threadIdx.x;
-    u[it] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < vec_per_matrix) {
-      u[it] = detail::momentum8(g[2 * it], g[2 * it + 1], m[2 * it], m[2 * it + 1], mu, nesterov);
-      const long long v = 2 * (mat + i);
-      __stcs(M + v, m[2 * it]);
-      __stcs(M + v + 1, m[2 * it + 1]);
-      U[mat + i] = u[it];
+    for (int q = 0; q < kHalf; ++q) {
+      const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (i < vec_per_matrix) {
+        u = detail::momentum8(g[2 * q], g[2 * q + 1], m[2 * q], m[2 * q + 1], mu, nesterov);
+        const long long v = 2 * (mat + i);
+        __stcs(M + v, m[2 * q]);
+        __stcs(M + v + 1, m[2 * q + 1]);
+        U[mat + i] = u;
+      }
+      acc += detail::sumsq_bf16x8(u);
     }
   }
   // The first product of the NS reads U: it may start as this grid drains.
   ptx::griddep_launch_dependents();
-  float acc = 0.0f;
-#pragma unroll
-  for (int it = 0; it < kNormVecPerThread; ++it) acc += detail::sumsq_bf16x8(u[it]);
 
   const float part = detail::block_sum_fixed(acc, red);
   if (threadIdx.x == 0) {
