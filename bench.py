@@ -428,6 +428,20 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / ne
     io_bytes = host_in.numel() * 2
     del hws
+    # The machine's host link, for reading e2e: one upload and one download of the
+    # whole stack between the same pinned buffers and device tensors, each
+    # alone, with CUDA events on the current stream.
+    link = {}
+    for name, dst, src in (("h2d", G, host_in), ("d2h", host_out, out)):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        link[name + "_gbs"] = io_bytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    link["copy_floor_ms"] = io_bytes / (min(link["h2d_gbs"], link["d2h_gbs"]) * 1e9) * 1e3
 
     # Spot parity of the timed call's output (untimed; matrix 0 vs the oracle).
     import oracle
@@ -479,7 +493,8 @@ def main():
         "clocks": clocks,
         "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                 "steps": ne, "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
-                "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same},
+                "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same,
+                "host_link": link},
         "parity": parity,
         "cpu_baseline": cpu,
         "per_shape": per_shape,
