@@ -468,3 +468,29 @@ def test_muon_step_workspace_and_launch_count():
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_muon_step_without_device_is_unsupported():
     assert _call_step() == _lib.ERR_UNSUPPORTED_DEVICE
+
+
+def test_header_compiles_as_c_and_cpp(tmp_path):
+    # The boundary is a C ABI: the header must stand alone in a C99 and a C++17
+    # translation unit that uses its types and entry points.
+    import shutil
+    import subprocess
+
+    cuda_inc = "/usr/local/cuda/include"
+    cc, cxx = shutil.which("gcc"), shutil.which("g++")
+    if not (cc and cxx and os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h"))):
+        pytest.skip("no host C compiler or CUDA headers")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "muon_ns.h"\n'
+                   "int main(void) {\n"
+                   "  muon_step_hparams h = {0.02f, 0.95f, 0.0f, 1.0f, 1};\n"
+                   "  muon_ns_stack s = {0, 0, 1, 8, 8};\n"
+                   "  size_t n = 0;\n"
+                   "  (void)h; (void)s;\n"
+                   "  return muon_ns_workspace_size(1, 8, 8, &n) + muon_step_workspace_size(1, 8, 8, &n);\n"
+                   "}\n")
+    inc = ["-I" + os.path.join(ROOT, "include"), "-I" + cuda_inc]
+    for cmd in ([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only"] + inc + [str(src)],
+                [cxx, "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++"] + inc + [str(src)]):
+        p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+        assert p.returncode == 0, p.stdout
