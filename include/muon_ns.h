@@ -452,6 +452,36 @@ int muon_momentum(float* M, const float* G, muon_bf16* U, int batch, int rows, i
 int muon_apply(float* W, const muon_bf16* O, int batch, int rows, int cols, const muon_step_hparams* hp,
                cudaStream_t stream);
 
+/* One stack of a grouped Muon step: `batch` matrices of rows x cols, device
+ * fp32 W and M (updated in place) and G, contiguous, 16-byte aligned, with
+ * this stack's hyperparameters. */
+typedef struct {
+  float* W;
+  float* M;
+  const float* G;
+  int batch;
+  int rows;
+  int cols;
+  muon_step_hparams hp;
+} muon_step_stack;
+
+/* Workspace bytes of muon_step_grouped(): the muon_step_ws() workspaces of
+ * the non-empty stacks, end to end, in order.  Checks the stacks as the call
+ * does (no device needed). */
+int muon_step_grouped_workspace_size(const muon_step_stack* stacks, int num_stacks, size_t* bytes);
+
+/* One Muon step over several stacks (an optimizer step's parameter groups of
+ * different shapes and hyperparameters; host array of num_stacks <= 64
+ * descriptors), with one NS setting (steps, coeffs, eps).  Each stack gets its
+ * momentum kernel; the NS products of all stacks then share launches as in
+ * muon_ns_grouped(), the last update of each writing its own W.  Results equal
+ * muon_step_ws() on each stack alone, bit for bit.  No W or M may overlap any
+ * stack's W, M or G (MUON_NS_ERR_INVALID_ARG); empty stacks are skipped.  The
+ * device error word is the first non-empty stack's, at the start of the
+ * workspace.  Errors otherwise as muon_step_ws(). */
+int muon_step_grouped(const muon_step_stack* stacks, int num_stacks, int steps, const float* coeffs, float eps,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Kernel launches of one muon_step_ws() call: 1 + 3 * steps (3 if steps == 0). */
 int muon_step_launches(int steps);
 

@@ -31,8 +31,10 @@ from .ns import (  # noqa: F401
     muon_apply,
     muon_momentum,
     muon_step,
+    muon_step_grouped,
     read_error,
     set_wait_budget,
+    step_grouped_workspace_size,
     step_launches,
     step_workspace_size,
     workspace_region,

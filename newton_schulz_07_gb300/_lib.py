@@ -45,6 +45,15 @@ class MuonStepHparams(ctypes.Structure):
 
 _php = ctypes.POINTER(MuonStepHparams)
 
+
+class MuonStepStack(ctypes.Structure):
+    """muon_step_stack of include/muon_ns.h."""
+    _fields_ = [("W", ctypes.c_void_p), ("M", ctypes.c_void_p), ("G", ctypes.c_void_p), ("batch", ctypes.c_int),
+                ("rows", ctypes.c_int), ("cols", ctypes.c_int), ("hp", MuonStepHparams)]
+
+
+_pss = ctypes.POINTER(MuonStepStack)
+
 # name -> (restype, argtypes); the exported C ABI, in header order.
 SIGNATURES = {
     "muon_ns_version": (ctypes.c_char_p, []),
@@ -77,6 +86,8 @@ SIGNATURES = {
     "muon_step_ws": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _php, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_momentum": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _vp]),
     "muon_apply": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _php, _vp]),
+    "muon_step_grouped_workspace_size": (_c_int, [_pss, _c_int, _psz]),
+    "muon_step_grouped": (_c_int, [_pss, _c_int, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_step_launches": (_c_int, [_c_int]),
     "muon_ns_launches_per_call": (_c_int, [_c_int]),
     "muon_ns_tile_count": (_c_ll, [_c_int, _c_int, _c_int, _c_int]),

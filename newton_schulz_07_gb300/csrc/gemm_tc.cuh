@@ -229,8 +229,10 @@ struct GroupArgs {
   // of storing the iterate, each output value o, rounded to bf16 as it would
   // be stored, updates the fp32 master in place,
   //   w_out[b][i][j] = w_decay * w_out[b][i][j] - w_lrs * o,
-  // with w_out laid out like the output ([batch][M][N], row stride ld).
+  // with w_out laid out like the output ([batch][M][N], row stride ld), and
+  // w_decay = 1 - lr wd, w_lrs = lr scale of this group's stack.
   float* w_out;
+  float w_decay, w_lrs;
 };
 
 // Counter increment per finished unit of the tile space, whatever the
@@ -265,7 +267,6 @@ struct GemmParams {
   // the previous grid only before it exits, so that its completion still
   // implies that of every earlier kernel in the stream.
   int dep_flags;
-  float w_decay, w_lrs;  // GroupArgs::w_out: 1 - lr wd and lr scale
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
 };
@@ -971,10 +972,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               const float w[4] = {__uint_as_float(wv[it].x), __uint_as_float(wv[it].y),
                                   __uint_as_float(wv[it].z), __uint_as_float(wv[it].w)};
               ptx::st_global_v4(wbase + static_cast<long long>(row) * G.ld + col,
-                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[0]), P.w_decay * w[0])),
-                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[1]), P.w_decay * w[1])),
-                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[2]), P.w_decay * w[2])),
-                                __float_as_uint(fmaf(-P.w_lrs, __uint_as_float(o4[3]), P.w_decay * w[3])));
+                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[0]), G.w_decay * w[0])),
+                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[1]), G.w_decay * w[1])),
+                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[2]), G.w_decay * w[2])),
+                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[3]), G.w_decay * w[3])));
             }
           }
           __syncwarp();  // the staging chunk is rewritten by the next chunk

@@ -431,8 +431,8 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     if (io[i].W != nullptr) {
       if (f32) return MUON_NS_ERR_INVALID_ARG;  // the Muon step runs the bf16 NS
       P->grp[i].w_out = io[i].W;
-      P->w_decay = io[i].w_decay;
-      P->w_lrs = io[i].w_lrs;
+      P->grp[i].w_decay = io[i].w_decay;
+      P->grp[i].w_lrs = io[i].w_lrs;
     }
     // Signals the update counter; waits for this step's polynomial.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + 2 * p.batch;
@@ -1437,6 +1437,127 @@ int muon_step_ws(float* W, float* M, const float* G, int batch, int rows, int co
   S.w_decay = decay;
   S.w_lrs = lrs;
   return run_ns_stacks(&S, 1, steps, abc, eps, reinterpret_cast<int*>(ws + L.error), d.sms, stream, true, true);
+}
+
+namespace {
+
+// One stack of a grouped Muon step, checked: its shape, scalars and layout.
+struct StepStack {
+  Problem p;
+  Layout L;
+  float decay, lrs;
+  size_t offset;  // of this stack's step workspace in the call's workspace
+};
+
+int check_step_stacks(const muon_step_stack* stacks, int num_stacks, StepStack* out, int* n_out, size_t* bytes) {
+  if (num_stacks < 0 || num_stacks > 64 || (num_stacks > 0 && !stacks)) return MUON_NS_ERR_INVALID_ARG;
+  int n = 0;
+  size_t off = 0;
+  for (int i = 0; i < num_stacks; ++i) {
+    const muon_step_stack& st = stacks[i];
+    StepStack& t = out[n];
+    bool empty;
+    int s = check_shape(st.batch, st.rows, st.cols, &t.p, &empty);
+    if (s != MUON_NS_OK) return s;
+    if ((s = check_hparams(&st.hp, &t.decay, &t.lrs)) != MUON_NS_OK) return s;
+    if (empty) continue;
+    if (!st.W || !st.M || !st.G) return MUON_NS_ERR_INVALID_ARG;
+    if (!aligned16(st.W) || !aligned16(st.M) || !aligned16(st.G)) return MUON_NS_ERR_ALIGNMENT;
+    t.L = make_layout(t.p);
+    t.offset = off;
+    off += step_ws_total(t.p, t.L);
+    ++n;
+  }
+  // W and M are written: neither may overlap any stack's W, M or G (its own
+  // W and M excepted, which are the same buffer).
+  auto range = [&](int i, int a, uintptr_t* lo, uintptr_t* hi) {
+    const void* ptr[3] = {stacks[i].W, stacks[i].M, stacks[i].G};
+    *lo = reinterpret_cast<uintptr_t>(ptr[a]);
+    *hi = *lo + 4 * static_cast<size_t>(stacks[i].batch) * stacks[i].rows * stacks[i].cols;
+  };
+  for (int i = 0; i < num_stacks; ++i) {
+    for (int a = 0; a < 2; ++a) {
+      uintptr_t lo, hi;
+      range(i, a, &lo, &hi);
+      if (lo == hi) continue;
+      for (int j = 0; j < num_stacks; ++j) {
+        for (int c = 0; c < 3; ++c) {
+          if (i == j && a == c) continue;
+          uintptr_t lo2, hi2;
+          range(j, c, &lo2, &hi2);
+          if (lo2 != hi2 && lo < hi2 && lo2 < hi) return MUON_NS_ERR_INVALID_ARG;
+        }
+      }
+    }
+  }
+  *n_out = n;
+  *bytes = off;
+  return MUON_NS_OK;
+}
+
+}  // namespace
+
+int muon_step_grouped_workspace_size(const muon_step_stack* stacks, int num_stacks, size_t* bytes) {
+  if (!bytes) return MUON_NS_ERR_INVALID_ARG;
+  StepStack S[64];
+  int n = 0;
+  return check_step_stacks(stacks, num_stacks, S, &n, bytes);
+}
+
+int muon_step_grouped(const muon_step_stack* stacks, int num_stacks, int steps, const float* coeffs, float eps,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  float abc[3];
+  int s = check_scalars(steps, coeffs, eps, abc);
+  if (s != MUON_NS_OK) return s;
+  StepStack T[64];
+  int n = 0;
+  size_t need = 0;
+  if ((s = check_step_stacks(stacks, num_stacks, T, &n, &need)) != MUON_NS_OK) return s;
+  if (n == 0) return MUON_NS_OK;
+  if (!workspace || workspace_bytes < need) return MUON_NS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_NS_ERR_ALIGNMENT;
+  DevInfo d;
+  if ((s = current_device_info(&d)) != MUON_NS_OK) return s;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  Stack S[64];
+  int k = 0;
+  for (int i = 0; i < num_stacks; ++i) {
+    const muon_step_stack& st = stacks[i];
+    if (st.batch == 0 || st.rows == 0 || st.cols == 0) continue;
+    const StepStack& t = T[k];
+    uint8_t* ws = base + t.offset;
+    uint16_t* U = reinterpret_cast<uint16_t*>(ws + step_u_offset(t.L));
+    // This stack's error word, tickets and counters in one memset.
+    if (cudaMemsetAsync(ws, 0, t.L.deps + 12 * static_cast<size_t>(t.p.batch), stream) != cudaSuccess)
+      return MUON_NS_ERR_CUDA;
+    if ((s = launch_momentum(t.p, t.L, st.G, st.M, U, st.hp.momentum, st.hp.nesterov, ws, stream)) != MUON_NS_OK)
+      return s;
+    if (steps == 0) {
+      uint16_t* O = reinterpret_cast<uint16_t*>(ws + t.L.x);
+      const dim3 grid(static_cast<unsigned>(t.L.chunks), static_cast<unsigned>(t.p.batch));
+      if (mns::launch_pdl(mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, stream,
+                          reinterpret_cast<const uint4*>(U), reinterpret_cast<uint4*>(O), t.p.R * t.p.C / 8,
+                          reinterpret_cast<const float*>(ws + t.L.norms), eps) != cudaSuccess)
+        return MUON_NS_ERR_CUDA;
+      if ((s = launch_apply(st.W, O, t.p.batch * t.p.R * t.p.C, t.decay, t.lrs, d.sms, stream)) != MUON_NS_OK)
+        return s;
+    }
+    Stack& q = S[k];
+    q.p = t.p;
+    q.L = t.L;
+    q.G = U;
+    q.out = U;
+    q.ws = ws;
+    q.cur = nullptr;
+    q.W = st.W;
+    q.w_decay = t.decay;
+    q.w_lrs = t.lrs;
+    ++k;
+  }
+  if (steps == 0) return MUON_NS_OK;
+  // Every kernel reports to the first stack's error word.
+  return run_ns_stacks(S, k, steps, abc, eps, reinterpret_cast<int*>(base + T[0].offset + T[0].L.error), d.sms,
+                       stream, true, true);
 }
 
 int muon_momentum(float* M, const float* G, muon_bf16* U, int batch, int rows, int cols, float momentum,

@@ -410,5 +410,54 @@ def muon_apply(W: torch.Tensor, O: torch.Tensor, lr: float, weight_decay: float 
                    "muon_apply")
 
 
+def _step_stacks(groups):
+    """ctypes array of muon_step_stack for a list of groups (dicts with W, M, G
+    and the step's hyperparameters: lr, and optionally momentum, nesterov,
+    weight_decay, scale)."""
+    arr = (_lib.MuonStepStack * max(len(groups), 1))()
+    for i, g in enumerate(groups):
+        W, M, G = g["W"], g["M"], g["G"]
+        for t, n in ((W, "W"), (M, "M"), (G, "G")):
+            _check_f32(t, n)
+            if t.shape != W.shape or t.device != W.device:
+                raise ValueError("W, M and G of a group must have one shape and device")
+        b, r, c = _shape3(W)
+        scale = g.get("scale")
+        hp = _hparams(g["lr"], g.get("momentum", 0.95), g.get("weight_decay", 0.0),
+                      default_scale(r, c) if scale is None else scale, g.get("nesterov", True))
+        arr[i] = _lib.MuonStepStack(W.data_ptr(), M.data_ptr(), G.data_ptr(), b, r, c, hp)
+    return arr
+
+
+def step_grouped_workspace_size(groups) -> int:
+    arr = _step_stacks(groups)
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.lib().muon_step_grouped_workspace_size(arr, len(groups), ctypes.byref(n)),
+               "muon_step_grouped_workspace_size")
+    return n.value
+
+
+def muon_step_grouped(groups, steps: int = 5, coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS,
+                      workspace: torch.Tensor | None = None) -> None:
+    """One Muon step over several parameter groups in one call, in place on
+    each group's W and M.  `groups` is a list of dicts with keys W, M, G (fp32
+    CUDA tensors of one shape per group, all on one device) and lr, and
+    optionally momentum (0.95), nesterov (True), weight_decay (0) and scale
+    (sqrt(max(1, rows / cols)))."""
+    groups = list(groups)
+    if not groups:
+        return
+    dev = groups[0]["W"].device
+    if any(g["W"].device != dev for g in groups):
+        raise ValueError("all groups must be on one device")
+    arr = _step_stacks(groups)
+    if workspace is None:
+        workspace = torch.empty(max(step_grouped_workspace_size(groups), 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.lib().muon_step_grouped(arr, len(groups), int(steps), _coeffs(coeffs), float(eps),
+                                                _ptr(workspace), workspace.numel(), _stream(dev)),
+                   "muon_step_grouped")
+
+
 def step_launches(steps: int) -> int:
     return _lib.lib().muon_step_launches(steps)

@@ -184,6 +184,33 @@ def test_step_captured_in_a_graph_equals_eager_steps():
     np.testing.assert_array_equal(Wd.cpu().numpy().view(np.uint32), We.cpu().numpy().view(np.uint32))
 
 
+@pytest.mark.parametrize("steps", [5, 0])
+def test_grouped_step_equals_separate_steps_bitwise(steps):
+    # An optimizer step's parameter groups: wide, tall (larger shape factor) and
+    # a long-contraction stack, each with its own hyperparameters, plus an empty
+    # group; one call equals one muon_step_ws call per group, bit for bit.
+    specs = [((3, 256, 512), dict(lr=0.02, momentum=0.95, weight_decay=0.01)),
+             ((2, 520, 264), dict(lr=0.05, momentum=0.9, nesterov=False)),
+             ((1, 1040, 1280), dict(lr=0.01, momentum=0.8, weight_decay=0.1, scale=0.7)),
+             ((0, 64, 128), dict(lr=0.02))]
+    base = []
+    for i, (shape, hp) in enumerate(specs):
+        base.append((f32_stack(shape, 30 + i), f32_stack(shape, 40 + i, 0.05), f32_stack(shape, 50 + i, 0.05), hp))
+    groups = []
+    for W, M, G, hp in base:
+        groups.append(dict(W=torch.from_numpy(W).cuda(), M=torch.from_numpy(M).cuda(), G=torch.from_numpy(G).cuda(), **hp))
+    ws = torch.empty(ns.step_grouped_workspace_size(groups), dtype=torch.uint8, device="cuda")
+    ns.muon_step_grouped(groups, steps=steps, workspace=ws)
+    torch.cuda.synchronize()
+    assert ns.read_error(ws) == 0
+    for (W, M, G, hp), g in zip(base, groups):
+        if W.shape[0] == 0:
+            continue
+        Ws, Ms = run_step(W, M, G, steps=steps, **hp)
+        np.testing.assert_array_equal(g["M"].cpu().numpy(), Ms)
+        np.testing.assert_array_equal(g["W"].cpu().numpy().view(np.uint32), Ws.view(np.uint32))
+
+
 @pytest.mark.slow
 def test_full_size_expert_stack_sampled():
     w = ns_inputs.WORKLOADS["experts_128x1536x2048"]

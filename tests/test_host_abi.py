@@ -494,3 +494,40 @@ def test_header_compiles_as_c_and_cpp(tmp_path):
                 [cxx, "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++"] + inc + [str(src)]):
         p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         assert p.returncode == 0, p.stdout
+
+
+def _step_stack_array(specs):
+    arr = (_lib.MuonStepStack * max(len(specs), 1))()
+    for i, (W, M, G, b, r, c) in enumerate(specs):
+        arr[i] = _lib.MuonStepStack(W, M, G, b, r, c, _lib.MuonStepHparams(0.02, 0.95, 0.0, 1.0, 1))
+    return arr
+
+
+def test_grouped_step_workspace_and_errors():
+    L = _lib.lib()
+    n = ctypes.c_size_t(0)
+    MB = 1 << 20
+    specs = [(1 * MB, 2 * MB, 3 * MB, 2, 64, 128), (4 * MB, 5 * MB, 6 * MB, 3, 136, 264), (0, 0, 0, 0, 64, 128)]
+    arr = _step_stack_array(specs)
+    assert L.muon_step_grouped_workspace_size(arr, 3, ctypes.byref(n)) == _lib.OK
+    assert n.value == ns.step_workspace_size(2, 64, 128) + ns.step_workspace_size(3, 136, 264)
+
+    def call(specs, wsb=1 << 30, ws=1 << 24):
+        a = _step_stack_array(specs)
+        return L.muon_step_grouped(a, len(specs), 5, None, ctypes.c_float(1e-7), ctypes.c_void_p(ws), wsb, None)
+
+    # The second stack's W overlaps the first stack's G (read while it is written).
+    assert call([specs[0], (3 * MB + 64, 5 * MB, 6 * MB, 3, 136, 264)]) == _lib.ERR_INVALID_ARG
+    # W and M of one stack overlap.
+    assert call([(1 * MB, 1 * MB + 16, 3 * MB, 2, 64, 128)]) == _lib.ERR_INVALID_ARG
+    assert call([(0, 2 * MB, 3 * MB, 2, 64, 128)]) == _lib.ERR_INVALID_ARG
+    assert call([(1 * MB + 4, 2 * MB, 3 * MB, 2, 64, 128)]) == _lib.ERR_ALIGNMENT
+    assert call([(1 * MB, 2 * MB, 3 * MB, 2, 60, 128)]) == _lib.ERR_ALIGNMENT
+    assert call(specs[:2], wsb=1024) == _lib.ERR_WORKSPACE
+    assert call(specs[:2], ws=(1 << 24) + 16) == _lib.ERR_ALIGNMENT
+    assert call([specs[2]]) == _lib.OK  # only an empty stack: nothing to do
+    assert L.muon_step_grouped(None, 1, 5, None, ctypes.c_float(1e-7), None, 0, None) == _lib.ERR_INVALID_ARG
+    big = (_lib.MuonStepStack * 65)()
+    assert L.muon_step_grouped(big, 65, 5, None, ctypes.c_float(1e-7), None, 0, None) == _lib.ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert call(specs[:2]) == _lib.ERR_UNSUPPORTED_DEVICE
