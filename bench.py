@@ -459,6 +459,9 @@ def main():
             per_shape[name] = time_workload(torch, ns, ow, dev, peaks)
         per_shape[w.name + "_fp32_mode"] = time_f32(torch, ns, w, dev, peaks)
         per_shape["muon_step_" + w.name.split("_", 1)[1]] = time_muon_step(torch, ns, w, dev, peaks)
+        step_mix = ["experts_16x1536x2048", "stack_128x2048x768", "tiny_4x256x512"]
+        per_shape["muon_step_grouped_" + "+".join(n.split("_", 1)[1] for n in step_mix)] = time_muon_step_grouped(
+            torch, ns, [ns_inputs.WORKLOADS[n] for n in step_mix], dev, peaks)
         for names in (["stack_32x7168x2048", "stack_128x2048x768"],
                       ["experts_16x1536x2048", "stack_128x2048x768", "tiny_4x256x512"]):
             per_shape["grouped_" + "+".join(n.split("_", 1)[1] for n in names)] = time_grouped(
@@ -664,6 +667,39 @@ def time_muon_step(torch, ns, w, dev, peaks, calls=20, warmup=3):
            "parity": parity, "device_error_word": ns.read_error(sws),
            "l2": "working set >> L2"}
     del G, W, M, sws, ws1, ws2, U, O
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_muon_step_grouped(torch, ns, wls, dev, peaks, calls=20, warmup=3):
+    """One Muon step over several parameter groups (fp32 W, M, G per stack) as
+    one muon_step_grouped call, against one muon_step_ws call per group,
+    interleaved call by call."""
+    gen = torch.Generator(device=dev).manual_seed(4321)
+    groups = []
+    for i, w in enumerate(wls):
+        G = torch.from_numpy(np.stack([ns_inputs.matrix_f32(w, k) for k in range(w.batch)])).to(dev)
+        groups.append(dict(W=torch.randn(G.shape, generator=gen, device=dev) * 0.02,
+                           M=torch.randn(G.shape, generator=gen, device=dev) * 0.02, G=G,
+                           lr=0.02 / (i + 1), momentum=0.95, weight_decay=0.01))
+    gws = torch.empty(ns.step_grouped_workspace_size(groups), dtype=torch.uint8, device=dev)
+    sws = [torch.empty(ns.step_workspace_size(*g["W"].shape), dtype=torch.uint8, device=dev) for g in groups]
+
+    def grouped():
+        ns.muon_step_grouped(groups, workspace=gws)
+
+    def separate():
+        for g, w in zip(groups, sws):
+            ns.muon_step(g["W"], g["M"], g["G"], g["lr"], momentum=g["momentum"], weight_decay=g["weight_decay"],
+                         workspace=w)
+
+    t = time_calls(torch, {"separate": separate, "grouped": grouped}, torch.cuda.current_stream(dev), calls, warmup)
+    g, sp = t["grouped"], t["separate"]
+    res = {"ms": g["median"], "ms_min": g["min"], "ms_max": g["max"], "calls": g["calls"],
+           "stacks": [w.name for w in wls], "api": "muon_step_grouped (one call)",
+           "separate_calls_ms": sp["median"], "separate_calls_ms_min": sp["min"],
+           "grouped_over_separate": g["median"] / sp["median"], "device_error_word": ns.read_error(gws)}
+    del groups, gws, sws
     torch.cuda.empty_cache()
     return res
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmuon_ns.so")
 
-SOURCES = ["muon_ns.cu", "gemm_sym.cu", "gemm_full.cu", "gemm_f32.cu", "gemm_wout.cu"]
+SOURCES = ["muon_ns.cu", "gemm_sym.cu", "gemm_full.cu", "gemm_f32.cu", "gemm_wout.cu", "gemm_wout_grp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

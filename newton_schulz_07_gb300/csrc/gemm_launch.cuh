@@ -49,7 +49,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // unit of the tile space.  Clusters are further limited to the number that
 // can be resident at once (the kernel is persistent).
 template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32 = false, int CL = 1,
-          bool SM2 = false, bool WOUT = false>
+          bool SM2 = false, int WOUT = 0>
 cudaError_t launch_tc_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Smem<SYM, EPI_WARPS, F32, SM2>::kSmemBytes;
   constexpr int kThreads = Epi<EPI_WARPS>::kCtaThreads;

@@ -32,7 +32,9 @@
 //         stage in both CTAs.  Half the B-operand bytes per CTA come from L2;
 //   WOUT  (update products only) the last update of a Muon step: the
 //         epilogue updates the fp32 master weights in place of storing the
-//         iterate (GroupArgs::w_out), prefetching their rows one chunk ahead;
+//         iterate (GroupArgs::w_out), prefetching their rows one chunk ahead,
+//         with the launch's factors (1, GemmParams::w_decay / w_lrs) or each
+//         group's own (2, GemmParams::w_decay_g / w_lrs_g);
 //   SM2   (CL == 2 only) the pair runs 2-SM MMAs instead: one thread of CTA 0
 //         issues M = 256 tcgen05.mma.cta_group::2 over A tiles held by both
 //         CTAs (128 rows each) and a B panel split in halves between them,
@@ -230,10 +232,16 @@ struct GroupArgs {
   // be stored, updates the fp32 master in place,
   //   w_out[b][i][j] = w_decay * w_out[b][i][j] - w_lrs * o,
   // with w_out laid out like the output ([batch][M][N], row stride ld), and
-  // w_decay = 1 - lr wd, w_lrs = lr scale of this group's stack.
+  // w_decay = 1 - lr wd, w_lrs = lr scale (GemmParams::w_decay / w_lrs, or
+  // w_decay_g / w_lrs_g for WOUT = 2).
   float* w_out;
-  float w_decay, w_lrs;
 };
+
+// The group arguments are read with a run-time group index: at 144 bytes each
+// entry starts on a 16-byte boundary.  Two more floats (152 bytes) measured
+// the fused Muon step 2.5 % slower on GB300, so per-group additions go to the
+// end of GemmParams instead.
+static_assert(sizeof(GroupArgs) % 16 == 0, "GroupArgs entries 16-byte aligned");
 
 // Counter increment per finished unit of the tile space, whatever the
 // launch's CTAs per unit and epilogue warps.
@@ -267,8 +275,13 @@ struct GemmParams {
   // the previous grid only before it exits, so that its completion still
   // implies that of every earlier kernel in the stream.
   int dep_flags;
+  // GroupArgs::w_out with one pair of factors for every group (WOUT = 1):
+  // 1 - lr wd and lr scale.
+  float w_decay, w_lrs;
   int* err;           // device error word, or nullptr
   long long budget;   // clock64 cycles per wait
+  // The same factors for each group (WOUT = 2).
+  float w_decay_g[kMaxGroups], w_lrs_g[kMaxGroups];
 };
 
 // Group owning global tile t (groups are few; a linear scan).
@@ -380,7 +393,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace detail
 
-template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, bool SM2 = false, bool WOUT = false>
+template <bool A_MN, bool B_MN, bool SYM, int EPI_WARPS, bool F32, int CL = 1, bool SM2 = false, int WOUT = 0>
 __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
     ns_tc_gemm(const __grid_constant__ GemmParams P) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
@@ -802,9 +815,12 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       // one chunk ahead; chunk 0 before the accumulator wait, which hides its
       // latency.  W is written by no other kernel of the call, so it may be
       // read early.
-      constexpr bool kW = WOUT;
+      constexpr bool kW = WOUT != 0;
       const bool wmode = kW && G.w_out != nullptr;
       float* wbase = wmode ? G.w_out + static_cast<long long>(b) * G.bstride : nullptr;
+      // The factors: the launch's (WOUT 1) or this group's (WOUT 2).
+      const float w_decay = WOUT == 2 ? P.w_decay_g[gr] : P.w_decay;
+      const float w_lrs = WOUT == 2 ? P.w_lrs_g[gr] : P.w_lrs;
       const int wr0 = I * kTileM + q * 32;  // first row of this warp
       uint4 wv[kW ? 8 : 1];
       auto load_w = [&](int cc, uint4 (&dst)[kW ? 8 : 1]) {
@@ -972,10 +988,10 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
               const float w[4] = {__uint_as_float(wv[it].x), __uint_as_float(wv[it].y),
                                   __uint_as_float(wv[it].z), __uint_as_float(wv[it].w)};
               ptx::st_global_v4(wbase + static_cast<long long>(row) * G.ld + col,
-                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[0]), G.w_decay * w[0])),
-                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[1]), G.w_decay * w[1])),
-                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[2]), G.w_decay * w[2])),
-                                __float_as_uint(fmaf(-G.w_lrs, __uint_as_float(o4[3]), G.w_decay * w[3])));
+                                __float_as_uint(fmaf(-w_lrs, __uint_as_float(o4[0]), w_decay * w[0])),
+                                __float_as_uint(fmaf(-w_lrs, __uint_as_float(o4[1]), w_decay * w[1])),
+                                __float_as_uint(fmaf(-w_lrs, __uint_as_float(o4[2]), w_decay * w[2])),
+                                __float_as_uint(fmaf(-w_lrs, __uint_as_float(o4[3]), w_decay * w[3])));
             }
           }
           __syncwarp();  // the staging chunk is rewritten by the next chunk

@@ -56,8 +56,13 @@ cudaError_t launch_full_kk(const GemmParams& p, PairMode mode, int max_k, int gr
 
 // The last update of a Muon step (GroupArgs::w_out): bf16 update products
 // whose epilogue writes the fp32 master weights; always 4 epilogue warps.
-cudaError_t launch_full_kmn_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
-cudaError_t launch_full_kk_w(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+// The factors are GemmParams::w_decay / w_lrs for every group, or with
+// `per_group` each group's GemmParams::w_decay_g / w_lrs_g.
+cudaError_t launch_full_kmn_w(const GemmParams& p, PairMode mode, int grid, bool per_group, cudaStream_t stream);
+cudaError_t launch_full_kk_w(const GemmParams& p, PairMode mode, int grid, bool per_group, cudaStream_t stream);
+// The per-group instantiations (gemm_wout_grp.cu).
+cudaError_t launch_full_kmn_wg(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
+cudaError_t launch_full_kk_wg(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);
 
 // The same for fp32 operands and outputs (tf32 tensor cores).
 cudaError_t launch_sym_kk_f32(const GemmParams& p, PairMode mode, int grid, cudaStream_t stream);

@@ -431,8 +431,8 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
     if (io[i].W != nullptr) {
       if (f32) return MUON_NS_ERR_INVALID_ARG;  // the Muon step runs the bf16 NS
       P->grp[i].w_out = io[i].W;
-      P->grp[i].w_decay = io[i].w_decay;
-      P->grp[i].w_lrs = io[i].w_lrs;
+      P->w_decay_g[i] = io[i].w_decay;
+      P->w_lrs_g[i] = io[i].w_lrs;
     }
     // Signals the update counter; waits for this step's polynomial.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep + 2 * p.batch;
@@ -458,8 +458,17 @@ int run_update(const StepIO* io, int ng, float alpha_x, float eps, bool round_ou
   if (f32)
     return to_status(T ? mns::launch_full_kk_f32(*P, mode, max_k, grid, st)
                        : mns::launch_full_kmn_f32(*P, mode, max_k, grid, st));
-  if (wout)
-    return to_status(T ? mns::launch_full_kk_w(*P, mode, grid, st) : mns::launch_full_kmn_w(*P, mode, grid, st));
+  if (wout) {
+    // One pair of factors for the launch unless the groups differ: the
+    // launch-wide kernel reads them without indexing the group arguments.
+    bool per_group = false;
+    for (int i = 1; i < ng; ++i)
+      per_group = per_group || io[i].w_decay != io[0].w_decay || io[i].w_lrs != io[0].w_lrs;
+    P->w_decay = io[0].w_decay;
+    P->w_lrs = io[0].w_lrs;
+    return to_status(T ? mns::launch_full_kk_w(*P, mode, grid, per_group, st)
+                       : mns::launch_full_kmn_w(*P, mode, grid, per_group, st));
+  }
   return to_status(T ? mns::launch_full_kk(*P, mode, max_k, grid, st)
                      : mns::launch_full_kmn(*P, mode, max_k, grid, st));
 }

@@ -184,15 +184,19 @@ def test_step_captured_in_a_graph_equals_eager_steps():
     np.testing.assert_array_equal(Wd.cpu().numpy().view(np.uint32), We.cpu().numpy().view(np.uint32))
 
 
-@pytest.mark.parametrize("steps", [5, 0])
-def test_grouped_step_equals_separate_steps_bitwise(steps):
+@pytest.mark.parametrize("steps,shared", [(5, False), (0, False), (5, True)])
+def test_grouped_step_equals_separate_steps_bitwise(steps, shared):
     # An optimizer step's parameter groups: wide, tall (larger shape factor) and
     # a long-contraction stack, each with its own hyperparameters, plus an empty
     # group; one call equals one muon_step_ws call per group, bit for bit.
+    # With `shared` the groups have the same factors (the last update's
+    # launch-wide form), otherwise each its own (the per-group form).
     specs = [((3, 256, 512), dict(lr=0.02, momentum=0.95, weight_decay=0.01)),
              ((2, 520, 264), dict(lr=0.05, momentum=0.9, nesterov=False)),
              ((1, 1040, 1280), dict(lr=0.01, momentum=0.8, weight_decay=0.1, scale=0.7)),
              ((0, 64, 128), dict(lr=0.02))]
+    if shared:
+        specs = [(shape, dict(lr=0.02, momentum=0.95, weight_decay=0.01, scale=1.0)) for shape, _ in specs]
     base = []
     for i, (shape, hp) in enumerate(specs):
         base.append((f32_stack(shape, 30 + i), f32_stack(shape, 40 + i, 0.05), f32_stack(shape, 50 + i, 0.05), hp))
