@@ -414,18 +414,21 @@ def main():
     # result, chunk by chunk with the copies overlapping the compute.
     host_out = torch.empty_like(host_in).pin_memory()
     hws = torch.empty(ns.host_workspace_size(*host_in.shape), dtype=torch.uint8, device=dev)
-    ne = min(args.steps, 20)
+    # Twenty calls back to back (each one's copies inside its own events), at
+    # least as many as the timed steps: the value is the median call, so one
+    # slow call on a shared host does not move it; the spread is recorded.
+    ne = max(min(args.steps, 100), 20)
     ns.muon_ns_host(host_in, out=host_out, workspace=hws, device=dev)
     torch.cuda.synchronize()
     e2e_same = bool(torch.equal(host_out, out.cpu()))  # the device-resident call's result, bit for bit
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ne):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(ne + 1)]
+    evs[0].record(stream)
+    for i in range(ne):
         ns.muon_ns_host(host_in, out=host_out, workspace=hws, device=dev, sync=False)
-    e1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / ne
+    e2e_calls = [evs[i].elapsed_time(evs[i + 1]) for i in range(ne)]
+    e2e_ms = statistics.median(e2e_calls)
     io_bytes = host_in.numel() * 2
     del hws
     # The machine's host link, for reading e2e: one upload and one download of the
@@ -495,7 +498,9 @@ def main():
         "breakdown": breakdown,
         "clocks": clocks,
         "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
-                "steps": ne, "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
+                "steps": ne, "stat": "median of back-to-back calls",
+                "ms_min": min(e2e_calls), "ms_max": max(e2e_calls), "ms_mean": statistics.fmean(e2e_calls),
+                "api": "newton_schulz_07_gb300.muon_ns_host -> muon_ns_host (C ABI, pinned host buffers)",
                 "largest_chunk_matrices": ns.host_chunk(*host_in.shape), "equals_device_result": e2e_same,
                 "host_link": link},
         "parity": parity,

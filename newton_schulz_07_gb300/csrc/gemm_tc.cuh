@@ -860,6 +860,15 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * kTileN);
       const int col_base = J * kTileN + c_begin * 32;  // first column of this warp
+      // Half storage keeps the diagonal 256 x 256 blocks whole, and a 2-SM
+      // unit on one has computed all of it (single-CTA tiles compute only the
+      // left half of an upper diagonal tile, N = 128): its warps store every
+      // chunk as computed, above the diagonal too, and mirror nothing.  (The
+      // tensor cores give bit-identical values at (i, j) and (j, i) of a
+      // product of symmetric operands: the same exact products summed in the
+      // same k order.)
+      const bool diag_direct =
+          SYM && SM2 && P.half_out && (col_base >> 8) == ((I * kTileM + q * 32) >> 8);
       // Addend coefficient: per row (row-indexed diagonal or none) ...
       float mscale = 1.0f;  // per-matrix scale of unscaled operands
       if (G.norms != nullptr) mscale = 1.0f / (ptx::ld_global_f32(G.norms + b) + P.eps);
@@ -891,7 +900,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
         const int gj0 = col_base + cc * 32;
 #pragma unroll
         for (int g = 0; g < kAV; ++g) dst[g] = make_uint4(0u, 0u, 0u, 0u);
-        if (addm == nullptr || !row_ok || gj0 >= G.N || (SYM && gj0 > gi)) return;
+        if (addm == nullptr || !row_ok || gj0 >= G.N || (SYM && gj0 > gi && !diag_direct)) return;
         const uint4* src = reinterpret_cast<const uint4*>(addm + (gi * G.ld + gj0) * EC::kBytes);
 #pragma unroll
         for (int g = 0; g < kAV; ++g)
@@ -909,7 +918,7 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
       for (int cc = 0; cc < n_chunks; ++cc) {
         const int gj0 = col_base + cc * 32;
         if (gj0 >= G.N) break;                   // warp-uniform
-        if (SYM && gj0 > warp_row_max) break;       // warp-uniform: above the diagonal
+        if (SYM && gj0 > warp_row_max && !diag_direct) break;  // warp-uniform: above the diagonal
         uint4 an[kAV];
         if (cc + 1 < kChunksPerWarp) load_addend(cc + 1, an);
         uint32_t v[32];
@@ -1088,8 +1097,9 @@ __global__ void __launch_bounds__(Epi<EPI_WARPS>::kCtaThreads, 1)
           put_begin();
           put(d, gj0, R0, 0);
           put_end();
-        } else if (gj0 < R0 && P.half_out && (gj0 >> 8) != (R0 >> 8)) {
-          // Half storage, outside the diagonal 256-block: the chunk alone.
+        } else if (diag_direct || (gj0 < R0 && P.half_out && (gj0 >> 8) != (R0 >> 8))) {
+          // Half storage: the chunk alone, outside the diagonal 256-blocks and
+          // (diag_direct) inside them.
           st_row(stg);
           put_begin();
           put(stg, gj0, R0, 0);
