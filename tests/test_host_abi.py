@@ -531,3 +531,48 @@ def test_grouped_step_workspace_and_errors():
     assert L.muon_step_grouped(big, 65, 5, None, ctypes.c_float(1e-7), None, 0, None) == _lib.ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert call(specs[:2]) == _lib.ERR_UNSUPPORTED_DEVICE
+
+
+def _half_store_writes(m, ts, sm2):
+    """Model of the symmetric epilogue's bulk stores with half storage: per
+    32-row warp block and 32-column chunk, the chunk alone outside the
+    diagonal 256-blocks; inside them, on 2-SM units (which compute the whole
+    block), every chunk as computed, and otherwise the chunk below the
+    diagonal plus its transpose, or the symmetrised diagonal block.  Counts
+    writes per 32 x 32 block."""
+    nb = -(-m // 32)
+    count = np.zeros((nb, nb), dtype=np.int32)
+    for _, I, J in ts:
+        for q in range(4):
+            R0 = I * TILE_M + q * 32
+            if R0 >= m:
+                continue  # all rows clipped
+            direct = sm2 and (J * TILE_N) >> 8 == R0 >> 8
+            for cc in range(TILE_N // 32):
+                gj0 = J * TILE_N + cc * 32
+                if gj0 >= m or (gj0 > R0 + 31 and not direct):
+                    break
+                if direct or (gj0 < R0 and gj0 >> 8 != R0 >> 8):
+                    count[R0 // 32, gj0 // 32] += 1
+                elif gj0 < R0:
+                    count[R0 // 32, gj0 // 32] += 1
+                    count[gj0 // 32, R0 // 32] += 1
+                else:
+                    count[R0 // 32, R0 // 32] += 1
+    return count
+
+
+@pytest.mark.parametrize("m", [8, 136, 256, 392, 640, 1000, 1040, 1536])
+@pytest.mark.parametrize("sm2", [False, True])
+def test_half_storage_writes_lower_triangle_and_diagonal_blocks_once(m, sm2):
+    # Half storage must hold every 32 x 32 block of the lower triangle and of
+    # the diagonal 256-blocks exactly once, and nothing else, whether the
+    # units are 2-SM pairs (direct stores inside the diagonal blocks) or
+    # single / multicast tiles (mirrored stores there).
+    nb = -(-m // 32)
+    bi, bj = np.meshgrid(np.arange(nb), np.arange(nb), indexing="ij")
+    want = ((bj <= bi) | ((bi * 32) >> 8 == (bj * 32) >> 8)).astype(np.int32)
+    units = unpair(tiles(2, 1, m, m), m)
+    np.testing.assert_array_equal(_half_store_writes(m, units, sm2), want)
+    if not sm2:
+        np.testing.assert_array_equal(_half_store_writes(m, tiles(0, 1, m, m), False), want)
