@@ -137,13 +137,9 @@ def test_gram_and_poly_stored_half_in_workspace(shape):
         assert np.linalg.norm(a[k][mask] - x0[mask]) / np.linalg.norm(x0[mask]) < 1.5e-2
 
 
-@pytest.mark.parametrize("shape", [(3, 392, 1000), (2, 1096, 1304), (2, 1304, 1096)])
-def test_call_equals_chain_of_step_calls_bitwise(shape):
-    # A whole call stores A and B half and orders its products per matrix
-    # through completion counters; the per-step entry points store them whole
-    # and wait for whole kernels.  The arithmetic is the same, so are the bits.
-    G = to_dev(random_bits(shape, seed=41))
-    out = ns.muon_ns(G, workspace=ns.alloc_workspace(*shape))
+def step_chain(G, shape):
+    """The 5-step NS of G through the per-step entry points (A and B stored
+    whole, each product waiting for the whole previous kernel)."""
     ws = ns.alloc_workspace(*shape)
     ns.muon_ns_normalize(G, ws, norms_only=True)
     off, nb = ns.workspace_region(*shape, ns._lib.WS_NORMS)
@@ -162,7 +158,44 @@ def test_call_equals_chain_of_step_calls_bitwise(shape):
         X = ns.muon_ns_update(X, B, a, diag=D, device_error=err, norms=first)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    np.testing.assert_array_equal(to_bits(out), to_bits(X))
+    return X
+
+
+@pytest.mark.parametrize("shape", [(3, 392, 1000), (2, 1096, 1304), (2, 1304, 1096)])
+def test_call_equals_chain_of_step_calls_bitwise(shape):
+    # A whole call stores A and B half and orders its products per matrix
+    # through completion counters; the per-step entry points store them whole
+    # and wait for whole kernels.  The arithmetic is the same, so are the bits.
+    G = to_dev(random_bits(shape, seed=41))
+    out = ns.muon_ns(G, workspace=ns.alloc_workspace(*shape))
+    np.testing.assert_array_equal(to_bits(out), to_bits(step_chain(G, shape)))
+
+
+def _sweep_shapes(n=16):
+    # Seeded draws of ragged shapes (multiples of 8): every fourth with both
+    # sides past 1024, so that all three products run as 2-SM pairs; the rest
+    # from 8 to 1104 (multicast pairs for short contractions, single tiles
+    # for tiny ones, wide and tall).
+    rng = np.random.default_rng(20261203)
+    out = []
+    for i in range(n):
+        lo, hi = (1032, 1304) if i % 4 == 0 else (8, 1104)
+        r, c = (8 * int(rng.integers(lo // 8, hi // 8 + 1)) for _ in range(2))
+        out.append((1 + int(rng.integers(0, 2)), r, c))
+    return out
+
+
+SWEEP = _sweep_shapes()
+
+
+@pytest.mark.parametrize("i,shape", list(enumerate(SWEEP)), ids=[f"{b}x{r}x{c}" for b, r, c in SWEEP])
+def test_random_shapes_vs_oracle_and_step_chain(i, shape):
+    bits = random_bits(shape, seed=900 + i)
+    out, _ = run_ws(bits)
+    errs = per_matrix_rel(to_f64(out), oracle_stack(bits))
+    tols = ns_tols(bits)
+    assert all(e <= t for e, t in zip(errs, tols)), (errs, tols)
+    np.testing.assert_array_equal(to_bits(out), to_bits(step_chain(to_dev(bits), shape)))
 
 
 def test_in_place_and_cached_workspace_agree():
