@@ -79,6 +79,12 @@ int check_shape(long long batch, long long rows, long long cols, Problem* p, boo
   return MUON_NS_OK;
 }
 
+// Grid of a per-matrix memory-bound kernel: x over a matrix's chunks, y over
+// the stack up to the hardware's 65535 (the kernels loop over the rest).
+dim3 batch_grid(long long chunks, long long batch) {
+  return dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(batch < 65535 ? batch : 65535));
+}
+
 Layout make_layout(const Problem& p) {
   Layout L;
   const size_t eb = p.f32 ? 4 : 2;  // bytes per element of G, X, A, B
@@ -480,16 +486,17 @@ int run_normalize(const Problem& p, const Layout& L, const void* G, void* X, flo
   const long long vec = p.R * p.C / (p.f32 ? 4 : 8);
   if (clear && cudaMemsetAsync(ws + L.tickets, 0, 4 * static_cast<size_t>(p.batch), st) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
-  const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
+  const dim3 grid = batch_grid(L.chunks, p.batch);
+  const int nb = static_cast<int>(p.batch);
   if (mns::launch_pdl(p.f32 ? mns::ns_norm_partial<true> : mns::ns_norm_partial<false>, grid, dim3(mns::kNormThreads), 0, st,
-                      reinterpret_cast<const uint4*>(G), vec, L.chunks,
+                      reinterpret_cast<const uint4*>(G), vec, L.chunks, nb,
                       reinterpret_cast<float*>(ws + L.partials),
                       reinterpret_cast<unsigned int*>(ws + L.tickets),
                       reinterpret_cast<float*>(ws + L.norms)) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   if (X == nullptr) return MUON_NS_OK;  // norms only
   if (mns::launch_pdl(p.f32 ? mns::ns_scale<true> : mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, st,
-                      reinterpret_cast<const uint4*>(G), reinterpret_cast<uint4*>(X), vec,
+                      reinterpret_cast<const uint4*>(G), reinterpret_cast<uint4*>(X), vec, nb,
                       reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
     return MUON_NS_ERR_CUDA;
   return MUON_NS_OK;
@@ -642,10 +649,10 @@ int run_ns_f32(const Problem& p, const Layout& L, const uint16_t* G, uint16_t* o
   // G^T into the orientation G lacks.
   {
     const dim3 grid(static_cast<unsigned>((p.C + 31) / 32), static_cast<unsigned>((p.R + 31) / 32),
-                    static_cast<unsigned>(p.batch));
+                    static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535));
     if (mns::launch_pdl(mns::ns_transpose_f32, grid, dim3(32, 8), 0, st,
                         reinterpret_cast<const float*>(G), reinterpret_cast<float*>(wide ? Y0 : W),
-                        static_cast<int>(p.R), static_cast<int>(p.C)) != cudaSuccess)
+                        static_cast<int>(p.R), static_cast<int>(p.C), static_cast<int>(p.batch)) != cudaSuccess)
       return MUON_NS_ERR_CUDA;
   }
   Problem pw = p;  // the Gram sees W: m x n, wide
@@ -1360,10 +1367,10 @@ size_t step_ws_total(const Problem& p, const Layout& L) {
 int launch_momentum(const Problem& p, const Layout& L, const float* G, float* M, uint16_t* U, float mu,
                     int nesterov, uint8_t* ws, cudaStream_t st) {
   const long long vec = p.R * p.C / 8;
-  const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
-  return to_status(mns::launch_pdl(mns::muon_momentum_norm, grid, dim3(mns::kNormThreads), 0, st,
-                                   reinterpret_cast<const float4*>(G), reinterpret_cast<float4*>(M),
-                                   reinterpret_cast<uint4*>(U), vec, L.chunks, mu, nesterov ? 1 : 0,
+  return to_status(mns::launch_pdl(mns::muon_momentum_norm, batch_grid(L.chunks, p.batch), dim3(mns::kNormThreads), 0,
+                                   st, reinterpret_cast<const float4*>(G), reinterpret_cast<float4*>(M),
+                                   reinterpret_cast<uint4*>(U), vec, L.chunks, static_cast<int>(p.batch), mu,
+                                   nesterov ? 1 : 0,
                                    reinterpret_cast<float*>(ws + L.partials),
                                    reinterpret_cast<unsigned int*>(ws + L.tickets),
                                    reinterpret_cast<float*>(ws + L.norms)));
@@ -1428,10 +1435,9 @@ int muon_step_ws(float* W, float* M, const float* G, int batch, int rows, int co
   if (steps == 0) {
     // O = U / (||U||_F + eps) into the iterate region, then the update.
     uint16_t* O = reinterpret_cast<uint16_t*>(ws + L.x);
-    const dim3 grid(static_cast<unsigned>(L.chunks), static_cast<unsigned>(p.batch));
-    if (mns::launch_pdl(mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, stream,
+    if (mns::launch_pdl(mns::ns_scale<false>, batch_grid(L.chunks, p.batch), dim3(mns::kNormThreads), 0, stream,
                         reinterpret_cast<const uint4*>(U), reinterpret_cast<uint4*>(O), p.R * p.C / 8,
-                        reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
+                        static_cast<int>(p.batch), reinterpret_cast<const float*>(ws + L.norms), eps) != cudaSuccess)
       return MUON_NS_ERR_CUDA;
     return launch_apply(W, O, p.batch * p.R * p.C, decay, lrs, d.sms, stream);
   }
@@ -1543,10 +1549,10 @@ int muon_step_grouped(const muon_step_stack* stacks, int num_stacks, int steps, 
       return s;
     if (steps == 0) {
       uint16_t* O = reinterpret_cast<uint16_t*>(ws + t.L.x);
-      const dim3 grid(static_cast<unsigned>(t.L.chunks), static_cast<unsigned>(t.p.batch));
-      if (mns::launch_pdl(mns::ns_scale<false>, grid, dim3(mns::kNormThreads), 0, stream,
-                          reinterpret_cast<const uint4*>(U), reinterpret_cast<uint4*>(O), t.p.R * t.p.C / 8,
-                          reinterpret_cast<const float*>(ws + t.L.norms), eps) != cudaSuccess)
+      if (mns::launch_pdl(mns::ns_scale<false>, batch_grid(t.L.chunks, t.p.batch), dim3(mns::kNormThreads), 0,
+                          stream, reinterpret_cast<const uint4*>(U), reinterpret_cast<uint4*>(O), t.p.R * t.p.C / 8,
+                          static_cast<int>(t.p.batch), reinterpret_cast<const float*>(ws + t.L.norms),
+                          eps) != cudaSuccess)
         return MUON_NS_ERR_CUDA;
       if ((s = launch_apply(st.W, O, t.p.batch * t.p.R * t.p.C, t.decay, t.lrs, d.sms, stream)) != MUON_NS_OK)
         return s;

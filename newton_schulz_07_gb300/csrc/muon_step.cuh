@@ -55,74 +55,79 @@ __device__ __forceinline__ uint4 momentum8(const float4 g0, const float4 g1, flo
 
 }  // namespace detail
 
-// grid (chunks, batch), kNormThreads threads.  G, M: fp32 [batch][R][C];
-// U: bf16 [batch][R][C]; vec_per_matrix = R * C / 8.  The CTA that takes the
-// last ticket of its matrix writes norms[b] (tickets zeroed beforehand).
+// grid (chunks, min(batch, 65535)), kNormThreads threads.  G, M: fp32
+// [batch][R][C]; U: bf16 [batch][R][C]; vec_per_matrix = R * C / 8.  A CTA
+// takes matrices blockIdx.y, blockIdx.y + gridDim.y, ... (the grid's y extent
+// stops at the hardware limit).  The CTA that takes the last ticket of its
+// matrix writes norms[b] (tickets zeroed beforehand).
 __global__ void __launch_bounds__(kNormThreads)
     muon_momentum_norm(const float4* __restrict__ G, float4* __restrict__ M, uint4* __restrict__ U,
-                       long long vec_per_matrix, int chunks, float mu, int nesterov,
+                       long long vec_per_matrix, int chunks, int batch, float mu, int nesterov,
                        float* __restrict__ partials, unsigned int* __restrict__ tickets,
                        float* __restrict__ norms) {
   __shared__ float red[kNormThreads / 32];
   __shared__ int is_last;
   ptx::griddep_wait();
-  const int b = blockIdx.y;
   const int chunk = blockIdx.x;
-  const long long mat = static_cast<long long>(b) * vec_per_matrix;
   const long long base = static_cast<long long>(chunk) * kNormChunkVec;
-
-  // The thread's vectors in two halves: the loads of a half (8 fp32 vectors
-  // in flight), then its arithmetic and stores.  Halves keep the registers
-  // low enough for several CTAs per SM; the norm still adds the vectors'
-  // sums of squares in the order ns_norm_partial does.
-  constexpr int kHalf = kNormVecPerThread / 2;
-  float acc = 0.0f;
+  for (int b = blockIdx.y; b < batch; b += gridDim.y) {
+    const long long mat = static_cast<long long>(b) * vec_per_matrix;
+    // The thread's vectors in two halves: the loads of a half (8 fp32 vectors
+    // in flight), then its arithmetic and stores.  Halves keep the registers
+    // low enough for several CTAs per SM; the norm still adds the vectors'
+    // sums of squares in the order ns_norm_partial does.
+    constexpr int kHalf = kNormVecPerThread / 2;
+    float acc = 0.0f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float4 g[2 * kHalf], m[2 * kHalf];
+    for (int h = 0; h < 2; ++h) {
+      float4 g[2 * kHalf], m[2 * kHalf];
 #pragma unroll
-    for (int q = 0; q < kHalf; ++q) {
-      const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
-      if (i < vec_per_matrix) {
-        const long long v = 2 * (mat + i);
-        g[2 * q] = __ldcs(G + v);
-        g[2 * q + 1] = __ldcs(G + v + 1);
-        m[2 * q] = M[v];
-        m[2 * q + 1] = M[v + 1];
+      for (int q = 0; q < kHalf; ++q) {
+        const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
+        if (i < vec_per_matrix) {
+          const long long v = 2 * (mat + i);
+          g[2 * q] = __ldcs(G + v);
+          g[2 * q + 1] = __ldcs(G + v + 1);
+          m[2 * q] = M[v];
+          m[2 * q + 1] = M[v + 1];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kHalf; ++q) {
+        const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (i < vec_per_matrix) {
+          u = detail::momentum8(g[2 * q], g[2 * q + 1], m[2 * q], m[2 * q + 1], mu, nesterov);
+          const long long v = 2 * (mat + i);
+          __stcs(M + v, m[2 * q]);
+          __stcs(M + v + 1, m[2 * q + 1]);
+          U[mat + i] = u;
+        }
+        acc += detail::sumsq_bf16x8(u);
       }
     }
-#pragma unroll
-    for (int q = 0; q < kHalf; ++q) {
-      const long long i = base + (h * kHalf + q) * kNormThreads + threadIdx.x;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (i < vec_per_matrix) {
-        u = detail::momentum8(g[2 * q], g[2 * q + 1], m[2 * q], m[2 * q + 1], mu, nesterov);
-        const long long v = 2 * (mat + i);
-        __stcs(M + v, m[2 * q]);
-        __stcs(M + v + 1, m[2 * q + 1]);
-        U[mat + i] = u;
-      }
-      acc += detail::sumsq_bf16x8(u);
-    }
-  }
-  // The first product of the NS reads U: it may start as this grid drains.
-  ptx::griddep_launch_dependents();
+    // The first product of the NS reads U: it may start as this grid drains
+    // (signalled once, after the CTA's first matrix).
+    if (b == static_cast<int>(blockIdx.y)) ptx::griddep_launch_dependents();
 
-  const float part = detail::block_sum_fixed(acc, red);
-  if (threadIdx.x == 0) {
-    partials[static_cast<long long>(b) * chunks + chunk] = part;
-    __threadfence();
-    const unsigned int ticket = atomicAdd(&tickets[b], 1u);
-    is_last = (ticket == static_cast<unsigned int>(chunks - 1)) ? 1 : 0;
+    const float part = detail::block_sum_fixed(acc, red);
+    if (threadIdx.x == 0) {
+      partials[static_cast<long long>(b) * chunks + chunk] = part;
+      __threadfence();
+      const unsigned int ticket = atomicAdd(&tickets[b], 1u);
+      is_last = (ticket == static_cast<unsigned int>(chunks - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (is_last) {  // CTA-uniform
+      __threadfence();
+      float s = 0.0f;
+      for (int i = threadIdx.x; i < chunks; i += kNormThreads)
+        s += __ldcg(&partials[static_cast<long long>(b) * chunks + i]);
+      const float total = detail::block_sum_fixed(s, red);
+      if (threadIdx.x == 0) norms[b] = sqrtf(total);
+    }
+    __syncthreads();  // is_last and red are rewritten for the next matrix
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  float s = 0.0f;
-  for (int i = threadIdx.x; i < chunks; i += kNormThreads)
-    s += __ldcg(&partials[static_cast<long long>(b) * chunks + i]);
-  const float total = detail::block_sum_fixed(s, red);
-  if (threadIdx.x == 0) norms[b] = sqrtf(total);
 }
 
 // W' = decay W - lrs O over n8 vectors of 8 elements (grid-stride).  W fp32,

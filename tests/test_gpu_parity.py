@@ -270,3 +270,43 @@ def test_error_tracks_the_rounding_model(shape):
     model = [per_matrix_rel(rounding_model.model_ns(g[k]), ref[k])[0] for k in range(shape[0])]
     for e, em in zip(got, model):
         assert abs(e - em) <= 0.1 * em, (got, model)
+
+
+def test_stack_beyond_the_grid_y_limit():
+    # More matrices than a grid's y extent allows (65535): the memory-bound
+    # kernels (norm, scale, the fp32 transpose, the Muon step's momentum) take
+    # the rest in further passes.  Every matrix is still computed as if alone:
+    # slices around the limit equal their own small-stack calls bit for bit,
+    # in bf16, in fp32 mode and through the Muon step, and sampled matrices
+    # match the oracle.
+    shape = (70000, 8, 16)
+    cuts = ((0, 3), (65533, 65538), (69997, 70000))
+    bits = random_bits(shape, seed=77)
+    out, _ = run_ws(bits)
+    got = to_bits(out)
+    for lo, hi in cuts:
+        part, _ = run_ws(bits[lo:hi])
+        np.testing.assert_array_equal(got[lo:hi], to_bits(part))
+    idx = [0, 65535, 69999]
+    errs = per_matrix_rel(to_f64(out)[idx], oracle_stack(bits[idx]))
+    tols = ns_tols(bits[idx])
+    assert all(e <= t for e, t in zip(errs, tols)), (errs, tols)
+
+    G32 = to_dev(bits).float()
+    out32 = ns.muon_ns_f32(G32)
+    for lo, hi in cuts:
+        part = ns.muon_ns_f32(G32[lo:hi].contiguous())
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out32[lo:hi].cpu().numpy().view(np.uint32), part.cpu().numpy().view(np.uint32))
+
+    W = (G32 * 3).contiguous()
+    M = (G32 * 0.5).contiguous()
+    Wb, Mb = W.clone(), M.clone()
+    ns.muon_step(Wb, Mb, G32, lr=0.02, momentum=0.9, weight_decay=0.01)
+    torch.cuda.synchronize()
+    for lo, hi in cuts:
+        Ws, Ms = W[lo:hi].clone(), M[lo:hi].clone()
+        ns.muon_step(Ws, Ms, G32[lo:hi].contiguous(), lr=0.02, momentum=0.9, weight_decay=0.01)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(Mb[lo:hi].cpu().numpy().view(np.uint32), Ms.cpu().numpy().view(np.uint32))
+        np.testing.assert_array_equal(Wb[lo:hi].cpu().numpy().view(np.uint32), Ws.cpu().numpy().view(np.uint32))
