@@ -310,3 +310,31 @@ def test_stack_beyond_the_grid_y_limit():
         torch.cuda.synchronize()
         np.testing.assert_array_equal(Mb[lo:hi].cpu().numpy().view(np.uint32), Ms.cpu().numpy().view(np.uint32))
         np.testing.assert_array_equal(Wb[lo:hi].cpu().numpy().view(np.uint32), Ws.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 1 << 20), (1, 1 << 20, 8)], ids=["8x1M", "1Mx8"])
+def test_longest_accepted_side_vs_oracle(shape):
+    # A side of 2^20, the longest the boundary accepts: the Gram's
+    # contraction runs 16384 k-blocks on one unit, the update writes 4096
+    # column tiles.
+    bits = random_bits(shape, seed=78)
+    out, _ = run_ws(bits)
+    errs = per_matrix_rel(to_f64(out), oracle_stack(bits))
+    tols = ns_tols(bits)
+    assert all(e <= t for e, t in zip(errs, tols)), (errs, tols)
+
+
+def test_largest_accepted_stack():
+    # 2^20 matrices, the most the boundary accepts: the norm pass loops 17
+    # times over the grid's y extent; slices equal their own calls bit for bit.
+    shape = (1 << 20, 8, 8)
+    bits = random_bits(shape, seed=79)
+    out, _ = run_ws(bits)
+    got = to_bits(out)
+    for lo, hi in ((0, 2), (524287, 524289), ((1 << 20) - 2, 1 << 20)):
+        part, _ = run_ws(bits[lo:hi])
+        np.testing.assert_array_equal(got[lo:hi], to_bits(part))
+    idx = [0, 65535, (1 << 20) - 1]
+    errs = per_matrix_rel(to_f64(out)[idx], oracle_stack(bits[idx]))
+    tols = ns_tols(bits[idx])
+    assert all(e <= t for e, t in zip(errs, tols)), (errs, tols)
