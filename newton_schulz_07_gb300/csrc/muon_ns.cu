@@ -320,13 +320,18 @@ int run_gram(const StepIO* io, int ng, float eps, int* err, int sms, cudaStream_
   for (int i = 0; i < ng; ++i)
     if (io[i].p.n > max_k) max_k = static_cast<int>(io[i].p.n);
   const mns::PairMode mode = mns::pair_mode(f32, max_k);
+  // A first step has no earlier product to wait on, only the norm kernel, so
+  // a launch that holds one waits for the whole previous kernel, whatever
+  // step its other groups are at.
+  bool by_counter = all_have_dep(io, ng);
+  for (int i = 0; i < ng; ++i) by_counter = by_counter && io[i].step > 0;
   for (int i = 0; i < ng; ++i) {
     const Problem& p = io[i].p;
     set_group(P, i, 1, p.batch, p.m, p.m, p.n, &total, f32, mode);
     P->grp[i].norms = io[i].norms;
     // Signals the Gram counter; waits for the previous step's update.
     if (io[i].dep != nullptr) P->grp[i].dep_sig = io[i].dep;
-    if (all_have_dep(io, ng) && io[i].step > 0) {
+    if (by_counter) {
       P->grp[i].dep_wait = io[i].dep + 2 * p.batch;
       P->grp[i].dep_target = static_cast<int>(io[i].step * dep_per_step_update(p));
       P->dep_flags = 1;

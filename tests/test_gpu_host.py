@@ -41,8 +41,11 @@ def test_host_path_equals_device_call_bitwise(chunk):
     np.testing.assert_array_equal(host_bits(out), device_ref(bits))
 
 
-@pytest.mark.parametrize("steps", [0, 1, 5])
+@pytest.mark.parametrize("steps", [0, 1, 2, 3, 4, 5, 7])
 def test_host_path_tall_input_and_step_counts(steps):
+    # Chunks of 1, 2, 1, 1 matrices (single-matrix chunks wait for whole
+    # kernels, the other one through counters); odd and even step counts end
+    # the iterate in different buffers of a chunk's slot.
     bits = random_bits((5, 264, 136), seed=52)
     G = host(bits)
     out = ns.muon_ns_host(G, steps=steps, chunk=2)
