@@ -310,9 +310,10 @@ def main():
     # Per-kernel breakdown, before the long timed loop (so that it runs in the
     # clock state of a kernel timed alone, which the burst peak describes; the
     # clock record decides): the same kernels in the same launch configuration
-    # as muon_ns_ws, through the per-step entry points, with CUDA events on the
-    # launching stream between launches.  Step 1 reads G and applies the
-    # per-matrix scale in its epilogues, as the whole call does.
+    # and storage form (A and B half-stored, MUON_NS_HALF) as muon_ns_ws,
+    # through the per-step entry points, with CUDA events on the launching
+    # stream between launches.  Step 1 reads G and applies the per-matrix
+    # scale in its epilogues, as the whole call does.
     nb = min(args.steps, 20)
     names = ["norm", "gram", "poly", "update"]
     acc = {k: 0.0 for k in names}
@@ -333,12 +334,12 @@ def main():
         ev[1].record(stream)
         src, cur = G, 0
         for s in range(5):
-            ns.muon_ns_gram(src, A=a_buf, device_error=err_word, norms=norms_t if s == 0 else None)
+            ns.muon_ns_gram(src, A=a_buf, device_error=err_word, norms=norms_t if s == 0 else None, half=True)
             ev[2 + 3 * s].record(stream)
-            ns.muon_ns_poly(a_buf, b, c, B=b_buf, diag=d_buf, device_error=err_word)
+            ns.muon_ns_poly(a_buf, b, c, B=b_buf, diag=d_buf, device_error=err_word, half=True)
             ev[3 + 3 * s].record(stream)
             ns.muon_ns_update(src, b_buf, a, Xn=x_bufs[cur], diag=d_buf, device_error=err_word,
-                              norms=norms_t if s == 0 else None)
+                              norms=norms_t if s == 0 else None, half=True)
             ev[4 + 3 * s].record(stream)
             src, cur = x_bufs[cur], 1 - cur
         torch.cuda.synchronize()
@@ -398,6 +399,7 @@ def main():
                 "avg_launch_ms": per_launch_ms[dominant]}
     norm_gbs = fl["norm_bytes"] / (per_launch_ms["norm"] * 1e-3) / 1e9
     breakdown = {
+        "storage": "A and B half-stored, as muon_ns_ws keeps them (per-step entry points with MUON_NS_HALF)",
         "per_launch_ms": per_launch_ms,
         "per_call_ms": share,
         "norm_hbm": {"achieved_gbs": norm_gbs, "peak_gbs": peaks["hbm_gbs"],

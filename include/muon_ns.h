@@ -27,9 +27,10 @@
  * A and B are symmetric and one triangle of each is computed (prime-rl PR
  * #3873, Summary item 1; Megatron-LM PR #6381 "Add --muon-use-syrk option",
  * Summary).  The per-step entry points mirror it, so the stored matrix is
- * bit-symmetric; the whole-call entry points mirror it only inside the
- * diagonal 256 x 256 blocks and the next product reads the rest of the upper
- * triangle transposed from the lower one.  The diagonal of B is kept in fp32
+ * bit-symmetric; the whole-call entry points store it half (MUON_NS_HALF
+ * below): whole inside the diagonal 256 x 256 blocks, the lower triangle
+ * elsewhere, and the next product reads the rest of the upper triangle
+ * transposed from the lower one.  The diagonal of B is kept in fp32
  * (B = D + O, O bf16 with a zero diagonal) and the update applies (a + D)
  * in its fp32 epilogue: the same arithmetic, with the part of B that
  * dominates near convergence kept out of bf16 rounding.
@@ -370,6 +371,28 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m
 int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
                    int batch, int rows, int cols, float a, const float* norms, float eps,
                    int* device_error, cudaStream_t stream);
+
+/* Half storage of the symmetric matrices, as the whole-call entry points keep
+ * them: A (or B) [batch][m][m] holds every diagonal 256 x 256 block whole
+ * (rows and columns 256 k .. 256 k + 255) and, outside them, only the lower
+ * triangle (i > j); the entries above the diagonal outside those blocks are
+ * neither written nor read.  A per-step chain in this form moves fewer bytes
+ * and runs the very kernels a whole call runs, with the same results bit for
+ * bit.  Each _ex function takes `flags` = 0 (as the function without _ex) or
+ * MUON_NS_HALF:
+ *   muon_ns_gram_ex    writes A half;
+ *   muon_ns_poly_ex    reads A half, writes B half;
+ *   muon_ns_update_ex  reads B half.
+ * Other flag bits return MUON_NS_ERR_INVALID_ARG.  The other arguments are as
+ * for muon_ns_gram(), muon_ns_poly() and muon_ns_update(). */
+#define MUON_NS_HALF 1
+int muon_ns_gram_ex(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols, const float* norms,
+                    float eps, int flags, int* device_error, cudaStream_t stream);
+int muon_ns_poly_ex(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b, float c,
+                    int flags, int* device_error, cudaStream_t stream);
+int muon_ns_update_ex(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn, int batch,
+                      int rows, int cols, float a, const float* norms, float eps, int flags, int* device_error,
+                      cudaStream_t stream);
 
 /* X = bf16(G * (1 / (||G_k||_F + eps))) exactly as muon_ns_normalize(), for
  * callers that cannot allocate device memory (plugins handed only their

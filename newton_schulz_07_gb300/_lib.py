@@ -20,6 +20,7 @@ ERR_CUDA = 5
 ERR_TIMEOUT = 6
 
 DEVERR_WAIT_TIMEOUT = 1  # bit of the device error word
+HALF = 1  # MUON_NS_HALF: per-step storage of A and B as whole calls keep them
 
 WS_TOTAL, WS_ERROR, WS_NORMS, WS_X, WS_GRAM, WS_POLY, WS_DIAG = range(7)
 
@@ -82,6 +83,9 @@ SIGNATURES = {
     "muon_ns_gram": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_f, _vp, _vp]),
     "muon_ns_poly": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_f, _c_f, _vp, _vp]),
     "muon_ns_update": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_f, _vp, _vp]),
+    "muon_ns_gram_ex": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_f, _c_int, _vp, _vp]),
+    "muon_ns_poly_ex": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_f, _c_f, _c_int, _vp, _vp]),
+    "muon_ns_update_ex": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _c_f, _c_int, _vp, _vp]),
     "muon_step_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _psz]),
     "muon_step_ws": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _php, _c_int, _pf, _c_f, _vp, _c_sz, _vp]),
     "muon_momentum": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _vp]),

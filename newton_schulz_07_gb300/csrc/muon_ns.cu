@@ -1278,12 +1278,13 @@ int muon_ns_normalize(const muon_bf16* G, muon_bf16* X, int batch, int rows, int
   return run_normalize(p, L, G, X, eps, static_cast<uint8_t*>(workspace), stream);
 }
 
-int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
-                 const float* norms, float eps, int* device_error, cudaStream_t stream) {
+int muon_ns_gram_ex(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols, const float* norms,
+                    float eps, int flags, int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, rows, cols, &p, &empty);
   if (s != MUON_NS_OK) return s;
+  if (flags & ~MUON_NS_HALF) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!X || !A) return MUON_NS_ERR_INVALID_ARG;
   if (norms && (!(eps >= 0.0f) || !std::isfinite(eps))) return MUON_NS_ERR_INVALID_ARG;
@@ -1295,16 +1296,22 @@ int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols
   io.X = X;
   io.A = A;
   io.norms = norms;
+  io.half = (flags & MUON_NS_HALF) != 0;
   return run_gram(&io, 1, eps, device_error, d.sms, stream);
 }
 
-int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
-                 float c, int* device_error, cudaStream_t stream) {
+int muon_ns_gram(const muon_bf16* X, muon_bf16* A, int batch, int rows, int cols,
+                 const float* norms, float eps, int* device_error, cudaStream_t stream) {
+  return muon_ns_gram_ex(X, A, batch, rows, cols, norms, eps, 0, device_error, stream);
+}
+
+int muon_ns_poly_ex(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b, float c,
+                    int flags, int* device_error, cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, m, m, &p, &empty);
   if (s != MUON_NS_OK) return s;
-  if (!std::isfinite(b) || !std::isfinite(c)) return MUON_NS_ERR_INVALID_ARG;
+  if (!std::isfinite(b) || !std::isfinite(c) || (flags & ~MUON_NS_HALF)) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!A || !B || A == B) return MUON_NS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(diag)) return MUON_NS_ERR_ALIGNMENT;
@@ -1315,17 +1322,23 @@ int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m
   io.A = const_cast<uint16_t*>(A);
   io.B = B;
   io.D = diag;
+  io.half = (flags & MUON_NS_HALF) != 0;
   return run_poly(&io, 1, b, c, device_error, d.sms, stream);
 }
 
-int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
-                   int batch, int rows, int cols, float a, const float* norms, float eps,
-                   int* device_error, cudaStream_t stream) {
+int muon_ns_poly(const muon_bf16* A, muon_bf16* B, float* diag, int batch, int m, float b,
+                 float c, int* device_error, cudaStream_t stream) {
+  return muon_ns_poly_ex(A, B, diag, batch, m, b, c, 0, device_error, stream);
+}
+
+int muon_ns_update_ex(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn, int batch,
+                      int rows, int cols, float a, const float* norms, float eps, int flags, int* device_error,
+                      cudaStream_t stream) {
   Problem p;
   bool empty;
   int s = check_shape(batch, rows, cols, &p, &empty);
   if (s != MUON_NS_OK) return s;
-  if (!std::isfinite(a)) return MUON_NS_ERR_INVALID_ARG;
+  if (!std::isfinite(a) || (flags & ~MUON_NS_HALF)) return MUON_NS_ERR_INVALID_ARG;
   if (norms && (!(eps >= 0.0f) || !std::isfinite(eps))) return MUON_NS_ERR_INVALID_ARG;
   if (empty) return MUON_NS_OK;
   if (!X || !B || !Xn || Xn == X || Xn == B) return MUON_NS_ERR_INVALID_ARG;
@@ -1340,7 +1353,14 @@ int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, mu
   io.D = const_cast<float*>(diag);
   io.norms = norms;
   io.Xn = Xn;
+  io.half = (flags & MUON_NS_HALF) != 0;
   return run_update(&io, 1, a, eps, false, device_error, d.sms, stream);
+}
+
+int muon_ns_update(const muon_bf16* X, const muon_bf16* B, const float* diag, muon_bf16* Xn,
+                   int batch, int rows, int cols, float a, const float* norms, float eps,
+                   int* device_error, cudaStream_t stream) {
+  return muon_ns_update_ex(X, B, diag, Xn, batch, rows, cols, a, norms, eps, 0, device_error, stream);
 }
 
 }  // extern "C"

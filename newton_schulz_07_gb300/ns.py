@@ -108,24 +108,28 @@ def muon_ns_normalize(G: torch.Tensor, workspace: torch.Tensor, eps: float = DEF
 
 
 def muon_ns_gram(X: torch.Tensor, A: torch.Tensor | None = None, device_error: torch.Tensor | None = None,
-                 norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS):
+                 norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS, half: bool = False):
     """A = X X^T (X^T X for tall X); with `norms` (fp32 [batch]) X is unscaled
-    and the Gram of X / (norms + eps) is computed."""
+    and the Gram of X / (norms + eps) is computed.  `half`: A stored half, as
+    whole calls keep it (diagonal 256-blocks whole, the lower triangle
+    elsewhere; MUON_NS_HALF)."""
     _check_bf16(X, "X")
     b, r, c = _shape3(X)
     m = min(r, c)
     if A is None:
         A = torch.empty((b, m, m) if X.dim() == 3 else (m, m), dtype=torch.bfloat16, device=X.device)
     with torch.cuda.device(X.device):
-        _lib.check(_lib.lib().muon_ns_gram(_ptr(X), _ptr(A), b, r, c, _ptr(norms), float(eps), _ptr(device_error),
-                                           _stream(X.device)), "muon_ns_gram")
+        _lib.check(_lib.lib().muon_ns_gram_ex(_ptr(X), _ptr(A), b, r, c, _ptr(norms), float(eps),
+                                              _lib.HALF if half else 0, _ptr(device_error), _stream(X.device)),
+                   "muon_ns_gram")
     return A
 
 
 def muon_ns_poly(A: torch.Tensor, b: float, c: float, B: torch.Tensor | None = None,
-                 diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None):
+                 diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None, half: bool = False):
     """B = b A + c A A.  With `diag` (fp32, batch*m elements) B's diagonal goes
-    there in fp32 and B's stored diagonal is zero."""
+    there in fp32 and B's stored diagonal is zero.  `half`: A read and B
+    written in half storage."""
     _check_bf16(A, "A")
     bt, m, m2 = _shape3(A)
     if m != m2:
@@ -134,16 +138,17 @@ def muon_ns_poly(A: torch.Tensor, b: float, c: float, B: torch.Tensor | None = N
         raise ValueError("diag must be a contiguous float32 tensor of batch * m elements")
     B = torch.empty_like(A) if B is None else B
     with torch.cuda.device(A.device):
-        _lib.check(_lib.lib().muon_ns_poly(_ptr(A), _ptr(B), _ptr(diag), bt, m, float(b), float(c),
-                                           _ptr(device_error), _stream(A.device)), "muon_ns_poly")
+        _lib.check(_lib.lib().muon_ns_poly_ex(_ptr(A), _ptr(B), _ptr(diag), bt, m, float(b), float(c),
+                                              _lib.HALF if half else 0, _ptr(device_error), _stream(A.device)),
+                   "muon_ns_poly")
     return B
 
 
 def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor | None = None,
                    diag: torch.Tensor | None = None, device_error: torch.Tensor | None = None,
-                   norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS):
+                   norms: torch.Tensor | None = None, eps: float = DEFAULT_EPS, half: bool = False):
     """X' = a X + B X (X' = a X + X B for tall X).  With `diag` from
-    muon_ns_poly, B = diag(D) + B_stored."""
+    muon_ns_poly, B = diag(D) + B_stored.  `half`: B read in half storage."""
     _check_bf16(X, "X")
     _check_bf16(B, "B")
     bt, r, c = _shape3(X)
@@ -152,8 +157,9 @@ def muon_ns_update(X: torch.Tensor, B: torch.Tensor, a: float, Xn: torch.Tensor 
         raise ValueError("diag must be a contiguous float32 tensor of batch * min(rows, cols) elements")
     Xn = torch.empty_like(X) if Xn is None else Xn
     with torch.cuda.device(X.device):
-        _lib.check(_lib.lib().muon_ns_update(_ptr(X), _ptr(B), _ptr(diag), _ptr(Xn), bt, r, c, float(a),
-                                             _ptr(norms), float(eps), _ptr(device_error), _stream(X.device)),
+        _lib.check(_lib.lib().muon_ns_update_ex(_ptr(X), _ptr(B), _ptr(diag), _ptr(Xn), bt, r, c, float(a),
+                                                _ptr(norms), float(eps), _lib.HALF if half else 0,
+                                                _ptr(device_error), _stream(X.device)),
                    "muon_ns_update")
     return Xn
 

@@ -137,9 +137,10 @@ def test_gram_and_poly_stored_half_in_workspace(shape):
         assert np.linalg.norm(a[k][mask] - x0[mask]) / np.linalg.norm(x0[mask]) < 1.5e-2
 
 
-def step_chain(G, shape):
+def step_chain(G, shape, half=False):
     """The 5-step NS of G through the per-step entry points (A and B stored
-    whole, each product waiting for the whole previous kernel)."""
+    whole, or half with `half`; each product waiting for the whole previous
+    kernel)."""
     ws = ns.alloc_workspace(*shape)
     ns.muon_ns_normalize(G, ws, norms_only=True)
     off, nb = ns.workspace_region(*shape, ns._lib.WS_NORMS)
@@ -153,22 +154,49 @@ def step_chain(G, shape):
     X = G
     for k in range(5):
         first = norms if k == 0 else None
-        ns.muon_ns_gram(X, A=A, device_error=err, norms=first)
-        ns.muon_ns_poly(A, bc, c, B=B, diag=D, device_error=err)
-        X = ns.muon_ns_update(X, B, a, diag=D, device_error=err, norms=first)
+        ns.muon_ns_gram(X, A=A, device_error=err, norms=first, half=half)
+        ns.muon_ns_poly(A, bc, c, B=B, diag=D, device_error=err, half=half)
+        X = ns.muon_ns_update(X, B, a, diag=D, device_error=err, norms=first, half=half)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return X
 
 
+@pytest.mark.parametrize("half", [False, True], ids=["full", "half"])
 @pytest.mark.parametrize("shape", [(3, 392, 1000), (2, 1096, 1304), (2, 1304, 1096)])
-def test_call_equals_chain_of_step_calls_bitwise(shape):
+def test_call_equals_chain_of_step_calls_bitwise(shape, half):
     # A whole call stores A and B half and orders its products per matrix
     # through completion counters; the per-step entry points store them whole
-    # and wait for whole kernels.  The arithmetic is the same, so are the bits.
+    # (or half, MUON_NS_HALF) and wait for whole kernels.  The arithmetic is
+    # the same, so are the bits.
     G = to_dev(random_bits(shape, seed=41))
     out = ns.muon_ns(G, workspace=ns.alloc_workspace(*shape))
-    np.testing.assert_array_equal(to_bits(out), to_bits(step_chain(G, shape)))
+    np.testing.assert_array_equal(to_bits(out), to_bits(step_chain(G, shape, half)))
+
+
+@pytest.mark.parametrize("shape", [(2, 392, 1000), (2, 1304, 1096), (1, 520, 264)])
+def test_half_storage_step_calls_store_what_full_storage_computes(shape):
+    # On the stored entries (the lower triangle and the diagonal 256-blocks)
+    # the half-stored A and B equal the fully stored ones bit for bit.
+    G = to_dev(random_bits(shape, seed=42))
+    b, m = shape[0], min(shape[1:])
+    mask = stored_mask(m)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    for half in (False, True):
+        A = torch.full((b, m, m), float("nan"), dtype=torch.bfloat16, device="cuda")
+        B = torch.full_like(A, float("nan"))
+        D = torch.empty((b, m), dtype=torch.float32, device="cuda")
+        Gs = G / 8  # small enough that A A stays well inside bf16 range
+        ns.muon_ns_gram(Gs, A=A, device_error=err, half=half)
+        ns.muon_ns_poly(A, -4.775, 2.0315, B=B, diag=D, device_error=err, half=half)
+        torch.cuda.synchronize()
+        res[half] = (to_bits(A), to_bits(B), D.cpu().numpy())
+    assert int(err.item()) == 0
+    for k in range(b):
+        for j in range(2):
+            np.testing.assert_array_equal(res[True][j][k][mask], res[False][j][k][mask])
+    np.testing.assert_array_equal(res[True][2].view(np.uint32), res[False][2].view(np.uint32))
 
 
 def _sweep_shapes(n=16):

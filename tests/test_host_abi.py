@@ -576,3 +576,15 @@ def test_half_storage_writes_lower_triangle_and_diagonal_blocks_once(m, sm2):
     np.testing.assert_array_equal(_half_store_writes(m, units, sm2), want)
     if not sm2:
         np.testing.assert_array_equal(_half_store_writes(m, tiles(0, 1, m, m), False), want)
+
+
+def test_half_storage_flags():
+    # Unknown flag bits are refused before the device is queried; the half
+    # flag itself is valid (without a GPU the call then stops at the device).
+    L = _lib.lib()
+    p = 1 << 20
+    assert L.muon_ns_gram_ex(p, p, 1, 256, 512, None, 1e-7, 2, None, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_poly_ex(p, p + 4096, None, 1, 256, -4.775, 2.0315, 4, None, None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_update_ex(p, p + 4096, None, p + 8192, 1, 256, 512, 3.4445, None, 1e-7, 3, None,
+                               None) == _lib.ERR_INVALID_ARG
+    assert L.muon_ns_gram_ex(p, p, 1, 256, 512, None, 1e-7, _lib.HALF, None, None) == _lib.ERR_UNSUPPORTED_DEVICE
