@@ -1157,15 +1157,6 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
     uint8_t* slot = base + 1024 + sl * H.slot;
     uint16_t* din = reinterpret_cast<uint16_t*>(slot + H.in);
     uint16_t* dout = reinterpret_cast<uint16_t*>(slot + H.out);
-    // Upload once the slot's previous chunk has finished reading its input.
-    if (i >= kHostSlots && cudaStreamWaitEvent(hp.up, hp.done[sl], 0) != cudaSuccess) return fail();
-    if (cudaMemcpyAsync(din, G_host + b0 * mat, bytes, cudaMemcpyHostToDevice, hp.up) != cudaSuccess ||
-        cudaEventRecord(hp.in[sl], hp.up) != cudaSuccess)
-      return fail();
-    // Compute once the input is up and the slot's previous output has been
-    // downloaded.
-    if (cudaStreamWaitEvent(stream, hp.in[sl], 0) != cudaSuccess) return fail();
-    if (i >= kHostSlots && cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
     Problem pi;
     check_shape(nb, rows, cols, &pi, &empty);
     Stack S;
@@ -1175,7 +1166,23 @@ int muon_ns_host(const muon_bf16* G_host, muon_bf16* out_host, int batch, int ro
     S.out = dout;
     S.ws = slot + H.ws;
     S.cur = nullptr;
-    if ((s = run_ns_stacks(&S, 1, steps, abc, eps, err, d.sms, stream)) != MUON_NS_OK) return s;
+    // Upload once the slot's previous chunk has finished reading its input;
+    // then, on the same stream and so beside the previous chunk's compute,
+    // clear this chunk's counters and take its norms (steps > 0), which
+    // keeps both off the compute stream.
+    if (i >= kHostSlots && cudaStreamWaitEvent(hp.up, hp.done[sl], 0) != cudaSuccess) return fail();
+    if (cudaMemcpyAsync(din, G_host + b0 * mat, bytes, cudaMemcpyHostToDevice, hp.up) != cudaSuccess) return fail();
+    if (steps > 0) {
+      if (cudaMemsetAsync(S.ws + S.L.tickets, 0, 16 * static_cast<size_t>(nb), hp.up) != cudaSuccess) return fail();
+      if ((s = run_normalize(pi, S.L, din, nullptr, eps, S.ws, hp.up, false)) != MUON_NS_OK) return s;
+    }
+    if (cudaEventRecord(hp.in[sl], hp.up) != cudaSuccess) return fail();
+    // Compute once the input (and its norms) are ready and the slot's
+    // previous output has been downloaded.
+    if (cudaStreamWaitEvent(stream, hp.in[sl], 0) != cudaSuccess) return fail();
+    if (i >= kHostSlots && cudaStreamWaitEvent(stream, hp.out[sl], 0) != cudaSuccess) return fail();
+    if ((s = run_ns_stacks(&S, 1, steps, abc, eps, err, d.sms, stream, steps > 0, steps > 0)) != MUON_NS_OK)
+      return s;
     if (cudaEventRecord(hp.done[sl], stream) != cudaSuccess) return fail();
     // Download once computed.
     if (cudaStreamWaitEvent(hp.down, hp.done[sl], 0) != cudaSuccess ||
