@@ -227,9 +227,9 @@ int muon_ns_grouped(const muon_ns_stack* stacks, int num_stacks, int steps, cons
  * Stacks held in host memory (e.g. optimizer states kept on the CPU).  The
  * stack is processed in chunks of `chunk` matrices: each chunk is uploaded,
  * orthogonalised and downloaded, and the copies of one chunk overlap the
- * compute of its neighbours (two chunks in flight; uploads and downloads run
- * on two streams the library creates once per device, the compute on
- * `stream`).  The matrices of a stack are independent (the leading axis is
+ * compute of its neighbours (two chunks in flight; uploads, each followed by
+ * its chunk's norm pass, and downloads run on two streams the library creates
+ * once per device, the products on `stream`).  The matrices of a stack are independent (the leading axis is
  * the batch, prime-rl PR #3873, Summary item 2), so the result equals
  * muon_ns_ws() on the whole stack bit for bit.  Host buffers should be
  * page-locked (cudaHostAlloc, or a pinned torch tensor) for the copies to
