@@ -227,3 +227,45 @@ def test_full_size_expert_stack_sampled():
         assert np.all(np.abs(Mn[k] - M_ref) <= 2.0 ** -23 * (0.95 * np.abs(M[k]) + np.abs(G[k])) + 1e-38)
         upd = 0.02 * np.linalg.norm(O_ref)
         assert np.linalg.norm(Wn[k] - W_ref) <= NS_TOL * upd + 4 * 2.0 ** -24 * np.linalg.norm(W[k])
+
+
+def _step_sweep(n=10):
+    # Seeded draws: ragged shapes (multiples of 8, wide and tall, every third
+    # with both sides past 1024 for 2-SM products), and hyperparameters.
+    rng = np.random.default_rng(20261204)
+    out = []
+    for i in range(n):
+        lo, hi = (1032, 1200) if i % 3 == 0 else (8, 880)
+        r, c = (8 * int(rng.integers(lo // 8, hi // 8 + 1)) for _ in range(2))
+        hp = dict(lr=float(rng.choice([0.002, 0.02, 0.2])), momentum=float(rng.choice([0.0, 0.8, 0.95])),
+                  nesterov=bool(rng.integers(0, 2)), weight_decay=float(rng.choice([0.0, 0.01, 0.1])))
+        out.append(((1 + int(rng.integers(0, 3)), r, c), hp))
+    return out
+
+
+STEP_SWEEP = _step_sweep()
+
+
+@pytest.mark.parametrize("i,case", list(enumerate(STEP_SWEEP)),
+                         ids=[f"{b}x{r}x{c}" for (b, r, c), _ in STEP_SWEEP])
+def test_random_steps_vs_oracle_and_chain(i, case):
+    # The fused step against the oracle step (M' to one fp32 rounding, W' to
+    # the NS tolerance on its update term) and bit for bit against its chain
+    # of separate kernels.
+    shape, hp = case
+    W, M, G = f32_stack(shape, 300 + i), f32_stack(shape, 400 + i, 0.05), f32_stack(shape, 500 + i, 0.05)
+    Wn, Mn = run_step(W, M, G, **hp)
+    Wc, Mc, _ = run_chain(W, M, G, **hp)
+    np.testing.assert_array_equal(Mn, Mc)
+    np.testing.assert_array_equal(Wn.view(np.uint32), Wc.view(np.uint32))
+    mu = hp["momentum"]
+    W_ref, M_ref, O_ref = oracle.muon_step(W, M, G, hp["lr"], mu, nesterov=hp["nesterov"],
+                                           weight_decay=hp["weight_decay"])
+    bound = 2.0 ** -23 * (np.abs(mu * M.astype(np.float64)) + np.abs(G)) + 1e-38
+    assert np.all(np.abs(Mn - M_ref) <= bound)
+    s = ns.default_scale(shape[1], shape[2])
+    tols = ns_tols(u_bits(M, G, mu, hp["nesterov"]))
+    for k in range(shape[0]):
+        upd = hp["lr"] * s * np.linalg.norm(O_ref[k])
+        err = np.linalg.norm(Wn[k] - W_ref[k])
+        assert err <= tols[k] * upd + 4 * 2.0 ** -24 * np.linalg.norm(W[k]), (k, err, upd, tols[k])
