@@ -59,6 +59,8 @@
  *     and nothing in the library exchanges data between GPUs.  Processes that
  *     drive more than one GPU are not a supported use.
  *   - Limits: batch, rows, cols <= 1<<20 and each matrix below 2^31 elements.
+ *     Magnitudes: ||G_k||_F below about 1.8e19 (the norm and the first Gram
+ *     accumulate in fp32); above it the norm overflows and the output is 0.
  *   - Errors found on the device (a bounded wait inside a kernel that ran out)
  *     set a device error word; the call that launched the kernels cannot
  *     see it, muon_ns_read_error() / muon_ns_cached_error() can.

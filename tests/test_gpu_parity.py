@@ -366,3 +366,15 @@ def test_largest_accepted_stack():
     errs = per_matrix_rel(to_f64(out)[idx], oracle_stack(bits[idx]))
     tols = ns_tols(bits[idx])
     assert all(e <= t for e, t in zip(errs, tols)), (errs, tols)
+
+
+@pytest.mark.parametrize("scale", [1e16, 1e-27], ids=["large", "small"])
+def test_extreme_magnitudes_vs_oracle(scale):
+    # Near the top of the accepted range (||G||_F about 4e18, below the fp32
+    # overflow of the norm's sum of squares at about 1.8e19) and far below
+    # eps (the norm underflows; eps dominates X = G / (norm + eps) in both
+    # implementations).
+    bits = random_bits((2, 256, 512), seed=81, scale=scale)
+    out, _ = run_ws(bits)
+    errs = per_matrix_rel(to_f64(out), oracle_stack(bits))
+    assert max(errs) <= NS_TOL, errs
