@@ -91,3 +91,11 @@ def test_host_path_workspace_too_small():
     ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
     with pytest.raises(ns.MuonNSError):
         ns.muon_ns_host(G, workspace=ws)
+
+
+def test_host_path_stack_beyond_the_grid_y_limit():
+    # 70,000 matrices in one chunk: the norm pass, which runs on the upload
+    # stream, loops past the grid's y limit; same bits as the device call.
+    bits = random_bits((70000, 8, 16), seed=56)
+    out = ns.muon_ns_host(host(bits))
+    np.testing.assert_array_equal(host_bits(out), device_ref(bits))
